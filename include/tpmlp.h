@@ -1,0 +1,185 @@
+/*
+ * tpmlp: the column->row tensor-parallel MLP block and the vocab-parallel
+ * cross-entropy, with T logical shards resident on one GPU.
+ *
+ * The method (page "一层 MLP 太宽而放不下时怎样切？列并行、行并行与块尾归约",
+ * zwjcode.cn, §01-§06):
+ *   Z^(r) = X W1^(r) + b1^(r),  H^(r) = act(Z^(r))      column shard r
+ *   P^(r) = H^(r) W2^(r)                                 row shard r, [N, D]
+ *   Y     = sum_r P^(r) + b2                             block-end SUM, b2 once
+ * with W1^(r) = W1[:, r*F/T : (r+1)*F/T] and W2^(r) = W2[r*F/T : (r+1)*F/T, :].
+ * Backward (§06): dH^(r) = dY W2^(r)^T, dZ^(r) = dH^(r) * act'(Z^(r)),
+ *   dW2^(r) = H^(r)^T dY, dW1^(r) = X^T dZ^(r), dX = sum_r dZ^(r) W1^(r)^T.
+ * Cross-entropy (page "unpurerationalist.github.io ... 3.4 TP for Embedding",
+ * LM-head bullets; Megatron TP chapter §7.8): per vocab shard k the local max
+ * m_k and sum s_k = sum exp(z - m_k); combined m = max_k m_k,
+ * S = sum_k s_k exp(m_k - m); loss_n = m + ln S - z[n, t_n].
+ *
+ * Conventions for every entry point:
+ * - All matrices are dense row-major. "[R, C]" means R rows of C elements,
+ *   row pitch C elements.
+ * - Tensor pointers are DEVICE pointers owned by the caller. Arrays of shard
+ *   pointers ("const void* const* W1") are HOST arrays of T device pointers;
+ *   the library reads them during the call only.
+ * - Element type is `dt` for X, W1, b1, W2, b2, Y, H, Z, dY, dX, dW1, dW2,
+ *   db1, db2. TPMLP_BF16 runs the tcgen05 tensor-core path (bf16 storage,
+ *   fp32 accumulation, fp32 partial sums); TPMLP_F32 runs a CUDA-core fp32
+ *   path (no TF32).
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream). The returned status reports argument errors and
+ *   launch failures synchronously; nothing is launched when an argument is
+ *   rejected. Errors found on the device (a bounded wait that expired, a
+ *   target id out of range) set a per-device error word that
+ *   tpmlp_check_device_error() reads.
+ * - The library allocates no device memory. Scratch space is the caller's
+ *   `workspace`; tpmlp_workspace_bytes() gives its size.
+ * - bf16 path alignment: every pointer 16-byte aligned and D % 8 == 0,
+ *   (F/T) % 8 == 0 (tensor-memory-access row pitches are multiples of 16
+ *   bytes); otherwise TPMLP_ERR_ALIGN.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TPMLP_MAX_SHARDS 16
+
+typedef enum {
+    TPMLP_OK = 0,
+    TPMLP_ERR_ARG = 1,        /* null pointer, bad enum, negative size; target id out of range (device) */
+    TPMLP_ERR_SHAPE = 2,      /* F % T != 0, V % T != 0, T outside [1, TPMLP_MAX_SHARDS], zero width */
+    TPMLP_ERR_ALIGN = 3,      /* bf16 path: pointer or row pitch not 16-byte aligned */
+    TPMLP_ERR_DTYPE = 4,      /* unknown element type */
+    TPMLP_ERR_CUDA = 5,       /* a CUDA runtime or driver call failed */
+    TPMLP_ERR_TIMEOUT = 6,    /* a bounded device-side wait expired (device error word) */
+    TPMLP_ERR_WORKSPACE = 7   /* workspace NULL or smaller than tpmlp_workspace_bytes() */
+} tpmlp_status;
+
+typedef enum { TPMLP_ACT_RELU = 0, TPMLP_ACT_GELU_TANH = 1 } tpmlp_act;
+typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
+
+/* How the T full-shape partial sums are combined (§04 block-end reduction).
+ * PARTIALS: each shard writes its fp32 partial P^(r) to the workspace, then a
+ *   vectorised reduce kernel sums them in shard order r = 0..T-1, adds b2 once
+ *   and casts (the single-GPU form of the all-reduce).
+ * SPLITK: the row GEMM runs its K loop over (r, k) into one fp32 accumulator,
+ *   so the shard sum never leaves the tensor-core accumulator; b2 is added
+ *   once in the epilogue. No workspace. */
+typedef enum { TPMLP_REDUCE_PARTIALS = 0, TPMLP_REDUCE_SPLITK = 1 } tpmlp_reduce_mode;
+
+typedef enum { TPMLP_OP_FORWARD = 0, TPMLP_OP_BACKWARD = 1 } tpmlp_op;
+
+/* Forward of one block (§01-§05).
+ *   X   [N, D]            input, replicated to every shard (read once)
+ *   W1  T x [D, F/T]      column shards of W1
+ *   b1  T x [F/T] or NULL column shards of b1 (NULL: no b1)
+ *   W2  T x [F/T, D]      row shards of W2
+ *   b2  [D] or NULL       added exactly once, after the shard sum
+ *   Y   [N, D]            output
+ *   H   T x [N, F/T]      output: act(Z^(r)) per shard (also the row GEMM's input)
+ *   Z   T x [N, F/T] or NULL  output: pre-activation Z^(r), needed by backward
+ * Workspace (PARTIALS only): partial P^(r), fp32 [N, D], starts at byte
+ * r * round_up(N*D*4, 256); it keeps the partials after the call.
+ * Errors: TPMLP_ERR_SHAPE if F % T != 0; TPMLP_ERR_WORKSPACE if mode is
+ * PARTIALS and workspace_bytes < tpmlp_workspace_bytes(FORWARD, ...). N = 0
+ * is valid and launches nothing. */
+tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
+                           const void* X, const void* const* W1, const void* const* b1,
+                           const void* const* W2, const void* b2, void* Y,
+                           void* const* H, void* const* Z, tpmlp_reduce_mode mode,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of one block (§06), for upstream gradient dY [N, D].
+ *   inputs: X, W1 (T x [D, F/T]), W2 (T x [F/T, D]), H and Z (T x [N, F/T],
+ *           as written by tpmlp_forward), dY [N, D]
+ *   outputs: dX [N, D] (summed over the T column shards), dW1 T x [D, F/T],
+ *            dW2 T x [F/T, D], db1 T x [F/T] or NULL, db2 [D] or NULL
+ * The workspace holds dZ^(r) (T x [N, F/T] of dt, shard r at byte
+ * r * round_up(N*(F/T)*sizeof(dt), 256)) and, in PARTIALS mode after those,
+ * the T fp32 dX partials (stride round_up(N*D*4, 256)). N = 0 writes zeros to
+ * dW1, dW2, db1, db2. */
+tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
+                            const void* X, const void* const* W1, const void* const* W2,
+                            const void* const* H, const void* const* Z, const void* dY,
+                            void* dX, void* const* dW1, void* const* dW2,
+                            void* const* db1, void* db2, tpmlp_reduce_mode mode,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Block-end reduction alone (§04-§05): Y = sum_{r=0}^{T-1} P^(r) + b2, summed
+ * in fp32 in shard order, b2 (element type dt, or NULL) added once, the result
+ * stored as dt.
+ *   partials  T x [N, D] fp32 (host array of T device pointers)
+ *   b2        [D] or NULL
+ *   Y         [N, D] */
+tpmlp_status tpmlp_block_reduce(tpmlp_dtype dt, int64_t N, int64_t D, int T,
+                                const float* const* partials, const void* b2, void* Y,
+                                void* stream);
+
+/* Vocab-parallel cross-entropy forward (see the header comment).
+ *   logits          [N, V] fp32; shard k owns columns [k*V/T, (k+1)*V/T)
+ *   targets         [N] int64 in [0, V)
+ *   loss_per_token  [N] fp32 out
+ *   loss_mean       [1] fp32 out, or NULL: (1/N) sum_n loss_n (fixed order)
+ *   argmax          [N] int32 out, or NULL: lowest index of the row maximum
+ *   target_owner    [N] int32 out, or NULL: t_n / (V/T)
+ * Errors: TPMLP_ERR_SHAPE if V % T != 0. A target outside [0, V) writes NaN
+ * for that token and sets TPMLP_ERR_ARG in the device error word. */
+tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
+                            const int64_t* targets, float* loss_per_token, float* loss_mean,
+                            int32_t* argmax, int32_t* target_owner, void* stream);
+
+/* Workspace bytes tpmlp_forward / tpmlp_backward need for these arguments
+ * (0 for a forward in SPLITK mode). Returns (size_t)-1 for invalid shapes. */
+size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                             tpmlp_reduce_mode mode);
+
+/* Human-readable name of a status code (static string). */
+const char* tpmlp_status_str(tpmlp_status s);
+
+/* Synchronizes `stream`, then reads and clears the current device's error
+ * word. Returns TPMLP_OK, TPMLP_ERR_TIMEOUT or TPMLP_ERR_ARG (device-side
+ * findings), or TPMLP_ERR_CUDA if the synchronization itself failed. */
+tpmlp_status tpmlp_check_device_error(void* stream);
+
+/* Upper bound, in nanoseconds, on every spin-wait inside the tensor-core
+ * kernels (default 2e9). A wait that runs out sets TPMLP_ERR_TIMEOUT in the
+ * device error word, the kernel drains its own copies, frees its tensor
+ * memory and returns. */
+void tpmlp_set_wait_timeout_ns(uint64_t ns);
+
+/* Failure-detection self test: launches one kernel whose thread waits, with
+ * the bounded wait above, on a barrier that nothing completes, so the wait
+ * always runs out after `timeout_ns`. The caller then sees TPMLP_ERR_TIMEOUT
+ * from tpmlp_check_device_error(). */
+tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* ---- instrumentation ---------------------------------------------------- */
+
+/* Number of kernels this library has launched in this process. */
+int64_t tpmlp_launch_count(void);
+
+typedef struct {
+    char name[48];       /* kernel kind, e.g. "tc_gemm_col_act" */
+    int64_t launches;
+    double total_ms;     /* sum of per-launch CUDA-event durations */
+} tpmlp_kernel_timing;
+
+/* When on, every launch is bracketed by CUDA events recorded on the stream
+ * the kernel is launched on. */
+void tpmlp_timing_enable(int on);
+/* Waits for the recorded events and writes up to max_entries aggregated
+ * per-kernel records; returns the number written (-1 on a CUDA error). */
+int tpmlp_timing_read(tpmlp_kernel_timing* out, int max_entries);
+/* Drops all recorded events and aggregates. */
+void tpmlp_timing_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

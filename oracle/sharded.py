@@ -60,6 +60,17 @@ def forward(X, W1, b1, W2, b2, kind, T, bias_per_shard=False):
     return {"H": H, "P": P, "Y": Y}
 
 
+def block_reduce(partials, b2):
+    """Block-end sum of full-shape partials, b2 added once (§04-§05):
+    Y = sum_r P^(r) + b2, summed in float64."""
+    out = as_f64(partials[0]).copy()
+    for p in partials[1:]:
+        out = out + as_f64(p)
+    if b2 is not None:
+        out = out + as_f64(b2)[None, :]
+    return out
+
+
 def backward_dx(X, W1, b1, W2, dY, kind, T):
     """Per-shard dX contributions dZ^(r) W1^(r)^T and their sum."""
     X, dY = as_f64(X), as_f64(dY)

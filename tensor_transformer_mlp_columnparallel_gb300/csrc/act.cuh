@@ -1,0 +1,42 @@
+// Elementwise activations of the block and their derivatives (device side).
+// ReLU: act'(0) = 0. GELU, tanh form (Hendrycks & Gimpel 2016):
+//   act(z)  = 0.5 z (1 + tanh(u)),  u = sqrt(2/pi) (z + 0.044715 z^3)
+//   act'(z) = 0.5 (1 + tanh(u)) + 0.5 z (1 - tanh(u)^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2)
+// tanh comes from CUDA's tanhf.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "tpmlp.h"
+
+namespace tpmlp {
+
+__device__ __forceinline__ float act_fwd(int act, float z) {
+    if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
+    const float c = 0.7978845608028654f;   // sqrt(2/pi)
+    const float u = c * fmaf(0.044715f * z, z * z, z);
+    return 0.5f * z * (1.f + tanhf(u));
+}
+
+__device__ __forceinline__ float act_grad(int act, float z) {
+    if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    const float c = 0.7978845608028654f;
+    const float z2 = z * z;
+    const float t = tanhf(c * fmaf(0.044715f * z, z2, z));
+    const float du = c * fmaf(3.f * 0.044715f, z2, 1.f);
+    return fmaf(0.5f * z * (1.f - t * t), du, 0.5f * (1.f + t));
+}
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& a, float& b) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    a = __low2float(h);
+    b = __high2float(h);
+}
+
+}  // namespace tpmlp

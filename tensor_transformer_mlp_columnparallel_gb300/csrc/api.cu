@@ -1,0 +1,518 @@
+// The C-ABI of include/tpmlp.h: argument checks, workspace layout, and the
+// order in which the steps of the block run on the caller's stream.
+//
+// Forward (page "一层 MLP 太宽而放不下时怎样切？", §02-§05), T logical shards:
+//   1. column GEMM, all shards in one grouped launch:
+//        Z^(r) = X W1^(r) + b1^(r), H^(r) = act(Z^(r))       (fused epilogue)
+//   2a. PARTIALS: row GEMM P^(r) = H^(r) W2^(r) into T fp32 buffers, then
+//       block_reduce Y = sum_r P^(r) + b2                       (b2 once)
+//   2b. SPLITK:   row GEMM with the shard sum in the K loop, Y = acc + b2
+// Backward (§06):
+//   1. dZ^(r) = (dY W2^(r)^T) * act'(Z^(r))                     (fused epilogue)
+//   2. dW2^(r) = H^(r)^T dY;  3. dW1^(r) = X^T dZ^(r)
+//   4. dX = sum_r dZ^(r) W1^(r)^T   (PARTIALS + block_reduce, or SPLITK)
+//   5. db1^(r) = sum_n dZ^(r), db2 = sum_n dY                   (if requested)
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+
+// ---------------------------------------------------------------------------
+// per-device services
+// ---------------------------------------------------------------------------
+
+__device__ int g_device_error;   // TPMLP_OK, or the first error a kernel recorded
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int64_t> g_launches{0};
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+}  // namespace
+
+int* device_error_word() {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_err_ptr[d] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[d] = static_cast<int*>(p);
+    }
+    return g_err_ptr[d];
+}
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int device_sm_count() {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 1;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_sms[d] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+        g_sms[d] = n > 0 ? n : 1;
+    }
+    return g_sms[d];
+}
+
+// ---------------------------------------------------------------------------
+// launch counting and event timing
+// ---------------------------------------------------------------------------
+
+namespace {
+struct TimingRec {
+    std::string name;
+    cudaEvent_t start, stop;
+};
+struct TimingAgg {
+    int64_t launches = 0;
+    double ms = 0.0;
+};
+std::mutex g_t_mu;
+bool g_timing = false;
+std::vector<TimingRec> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+std::map<std::string, TimingAgg> g_agg;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+}  // namespace
+
+LaunchScope::LaunchScope(const char* name, cudaStream_t s)
+    : name_(name ? name : "?"), s_(s), start_(nullptr), stop_(nullptr) {
+    g_launches.fetch_add(1);
+    std::lock_guard<std::mutex> lk(g_t_mu);
+    if (!g_timing) return;
+    start_ = take_event();
+    stop_ = take_event();
+    if (start_ == nullptr || stop_ == nullptr) {
+        start_ = stop_ = nullptr;
+        return;
+    }
+    cudaEventRecord(start_, s_);
+}
+
+LaunchScope::~LaunchScope() {
+    if (start_ == nullptr) return;
+    std::lock_guard<std::mutex> lk(g_t_mu);
+    cudaEventRecord(stop_, s_);
+    g_pending.push_back(TimingRec{name_, start_, stop_});
+}
+
+// ---------------------------------------------------------------------------
+// argument checks
+// ---------------------------------------------------------------------------
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+tpmlp_status check_dims(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act) {
+    if (dt != TPMLP_F32 && dt != TPMLP_BF16) return TPMLP_ERR_DTYPE;
+    if (act != TPMLP_ACT_RELU && act != TPMLP_ACT_GELU_TANH) return TPMLP_ERR_ARG;
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (D <= 0 || F <= 0 || T < 1 || T > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;
+    if (F % T != 0) return TPMLP_ERR_SHAPE;
+    if (N > 0x7fffffffLL || D > 0x7fffffffLL || F > 0x7fffffffLL) return TPMLP_ERR_SHAPE;
+    if (dt == TPMLP_BF16 && (D % 8 != 0 || (F / T) % 8 != 0)) return TPMLP_ERR_ALIGN;
+    return TPMLP_OK;
+}
+
+// every entry of a shard-pointer array present (and 16-byte aligned on the bf16 path)
+tpmlp_status check_shards(const void* const* a, int T, bool bf16) {
+    if (a == nullptr) return TPMLP_ERR_ARG;
+    for (int r = 0; r < T; ++r) {
+        if (a[r] == nullptr) return TPMLP_ERR_ARG;
+        if (bf16 && !aligned16(a[r])) return TPMLP_ERR_ALIGN;
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status check_ptr(const void* p, bool bf16) {
+    if (p == nullptr) return TPMLP_ERR_ARG;
+    if (bf16 && !aligned16(p)) return TPMLP_ERR_ALIGN;
+    return TPMLP_OK;
+}
+
+#define TPMLP_TRY(expr)                      \
+    do {                                     \
+        const tpmlp_status _s = (expr);      \
+        if (_s != TPMLP_OK) return _s;       \
+    } while (0)
+
+size_t partials_bytes(int64_t N, int64_t D, int T) { return (size_t)T * round256((size_t)N * D * 4); }
+size_t dz_bytes(tpmlp_dtype dt, int64_t N, int64_t Fs, int T) {
+    return (size_t)T * round256((size_t)N * Fs * (dt == TPMLP_BF16 ? 2 : 4));
+}
+
+tpmlp_status run_gemm(tpmlp_dtype dt, const GemmProblem& p, cudaStream_t s) {
+    return dt == TPMLP_BF16 ? run_gemm_tc(p, s) : run_gemm_simt(p, s);
+}
+
+GemmProblem problem(int M, int N, int K, int G, int fold, int64_t lda, int a_mn, int64_t ldb,
+                    int b_mn, const char* name) {
+    GemmProblem p;
+    memset(&p, 0, sizeof(p));
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.G = G;
+    p.fold = fold;
+    p.lda = lda;
+    p.a_mn = a_mn;
+    p.ldb = ldb;
+    p.b_mn = b_mn;
+    p.name = name;
+    return p;
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+extern "C" {
+
+size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                             tpmlp_reduce_mode mode) {
+    if (check_dims(dt, N, D, F, T, TPMLP_ACT_RELU) == TPMLP_ERR_SHAPE || N < 0 || T < 1)
+        return (size_t)-1;
+    if (dt != TPMLP_F32 && dt != TPMLP_BF16) return (size_t)-1;
+    const size_t part = mode == TPMLP_REDUCE_PARTIALS ? partials_bytes(N, D, T) : 0;
+    if (op == TPMLP_OP_FORWARD) return part;
+    if (op == TPMLP_OP_BACKWARD) return dz_bytes(dt, N, F / T, T) + part;
+    return (size_t)-1;
+}
+
+tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
+                           const void* X, const void* const* W1, const void* const* b1,
+                           const void* const* W2, const void* b2, void* Y, void* const* H,
+                           void* const* Z, tpmlp_reduce_mode mode, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    TPMLP_TRY(check_dims(dt, N, D, F, T, act));
+    if (mode != TPMLP_REDUCE_PARTIALS && mode != TPMLP_REDUCE_SPLITK) return TPMLP_ERR_ARG;
+    if (N == 0) return TPMLP_OK;   // every output is empty
+    const bool bf = dt == TPMLP_BF16;
+    TPMLP_TRY(check_ptr(X, bf));
+    TPMLP_TRY(check_ptr(Y, bf));
+    TPMLP_TRY(check_shards(W1, T, bf));
+    TPMLP_TRY(check_shards(W2, T, bf));
+    TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(H), T, bf));
+    if (b1 != nullptr) TPMLP_TRY(check_shards(b1, T, bf));
+    if (Z != nullptr) TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(Z), T, bf));
+    if (b2 != nullptr) TPMLP_TRY(check_ptr(b2, bf));
+    const size_t need = tpmlp_workspace_bytes(TPMLP_OP_FORWARD, dt, N, D, F, T, mode);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need) return TPMLP_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Fs = (int)(F / T);
+    const int f32 = bf ? 0 : 1;
+
+    // 1. column shards: H^(r) = act(X W1^(r) + b1^(r)), Z^(r) saved
+    GemmProblem col = problem((int)N, Fs, (int)D, T, 0, D, 0, Fs, 1, "col_gemm_bias_act");
+    col.epi.kind = EPI_ACT;
+    col.epi.act = act;
+    col.epi.out_f32 = f32;
+    col.epi.ldc = Fs;
+    col.epi.ldaux = Fs;
+    for (int r = 0; r < T; ++r) {
+        col.A[r] = X;
+        col.B[r] = W1[r];
+        col.epi.C[r] = H[r];
+        col.epi.bias[r] = b1 ? b1[r] : nullptr;
+        col.epi.aux[r] = Z ? Z[r] : nullptr;
+    }
+    TPMLP_TRY(run_gemm(dt, col, s));
+
+    // 2. row shards and the block-end sum
+    if (mode == TPMLP_REDUCE_PARTIALS) {
+        const size_t stride = round256((size_t)N * D * 4);
+        const float* parts[kMaxG];
+        GemmProblem row = problem((int)N, (int)D, Fs, T, 0, Fs, 0, D, 1, "row_gemm_partials");
+        row.epi.kind = EPI_STORE;
+        row.epi.out_f32 = 1;
+        row.epi.ldc = D;
+        for (int r = 0; r < T; ++r) {
+            float* pr = reinterpret_cast<float*>(static_cast<char*>(workspace) + r * stride);
+            row.A[r] = H[r];
+            row.B[r] = W2[r];
+            row.epi.C[r] = pr;
+            parts[r] = pr;
+        }
+        TPMLP_TRY(run_gemm(dt, row, s));
+        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s, "block_reduce_bias"));
+    } else {
+        GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1, "row_gemm_splitk_bias");
+        row.epi.kind = EPI_STORE;
+        row.epi.out_f32 = f32;
+        row.epi.ldc = D;
+        row.epi.C[0] = Y;
+        row.epi.bias[0] = b2;
+        for (int r = 0; r < T; ++r) {
+            row.A[r] = H[r];
+            row.B[r] = W2[r];
+        }
+        TPMLP_TRY(run_gemm(dt, row, s));
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
+                            const void* X, const void* const* W1, const void* const* W2,
+                            const void* const* H, const void* const* Z, const void* dY, void* dX,
+                            void* const* dW1, void* const* dW2, void* const* db1, void* db2,
+                            tpmlp_reduce_mode mode, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    TPMLP_TRY(check_dims(dt, N, D, F, T, act));
+    if (mode != TPMLP_REDUCE_PARTIALS && mode != TPMLP_REDUCE_SPLITK) return TPMLP_ERR_ARG;
+    const bool bf = dt == TPMLP_BF16;
+    TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(dW1), T, bf));
+    TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(dW2), T, bf));
+    if (db1 != nullptr) TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(db1), T, bf));
+    if (db2 != nullptr) TPMLP_TRY(check_ptr(db2, bf));
+    if (N > 0) {   // with no tokens, X, H, Z, dY, dX and the workspace are empty
+        TPMLP_TRY(check_ptr(X, bf));
+        TPMLP_TRY(check_ptr(dY, bf));
+        TPMLP_TRY(check_ptr(dX, bf));
+        TPMLP_TRY(check_shards(W1, T, bf));
+        TPMLP_TRY(check_shards(W2, T, bf));
+        TPMLP_TRY(check_shards(H, T, bf));
+        TPMLP_TRY(check_shards(Z, T, bf));
+        const size_t need = tpmlp_workspace_bytes(TPMLP_OP_BACKWARD, dt, N, D, F, T, mode);
+        if (workspace == nullptr || workspace_bytes < need) return TPMLP_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Fs = (int)(F / T);
+    const int f32 = bf ? 0 : 1;
+    const size_t esz = bf ? 2 : 4;
+
+    if (N == 0) {
+        // sums over an empty token set
+        for (int r = 0; r < T; ++r) {
+            if (cudaMemsetAsync(dW1[r], 0, (size_t)D * Fs * esz, s) != cudaSuccess ||
+                cudaMemsetAsync(dW2[r], 0, (size_t)Fs * D * esz, s) != cudaSuccess)
+                return TPMLP_ERR_CUDA;
+            if (db1 && cudaMemsetAsync(db1[r], 0, (size_t)Fs * esz, s) != cudaSuccess)
+                return TPMLP_ERR_CUDA;
+        }
+        if (db2 && cudaMemsetAsync(db2, 0, (size_t)D * esz, s) != cudaSuccess) return TPMLP_ERR_CUDA;
+        return TPMLP_OK;
+    }
+
+    const size_t dz_stride = round256((size_t)N * Fs * esz);
+    void* dZ[kMaxG];
+    for (int r = 0; r < T; ++r) dZ[r] = static_cast<char*>(workspace) + r * dz_stride;
+
+    // 1. dZ^(r) = (dY W2^(r)^T) * act'(Z^(r)); B(k, n) = W2^(r)[n, k]: K-major
+    GemmProblem g1 = problem((int)N, Fs, (int)D, T, 0, D, 0, D, 0, "bwd_dz_gemm_dact");
+    g1.epi.kind = EPI_DACT;
+    g1.epi.act = act;
+    g1.epi.out_f32 = f32;
+    g1.epi.ldc = Fs;
+    g1.epi.ldaux = Fs;
+    for (int r = 0; r < T; ++r) {
+        g1.A[r] = dY;
+        g1.B[r] = W2[r];
+        g1.epi.C[r] = dZ[r];
+        g1.epi.aux[r] = const_cast<void*>(Z[r]);
+    }
+    TPMLP_TRY(run_gemm(dt, g1, s));
+
+    // 2. dW2^(r) = H^(r)^T dY: A(m, k) = H^(r)[k, m] (MN-major), B(k, n) = dY[k, n]
+    GemmProblem g2 = problem(Fs, (int)D, (int)N, T, 0, Fs, 1, D, 1, "bwd_dw2_gemm");
+    g2.epi.kind = EPI_STORE;
+    g2.epi.out_f32 = f32;
+    g2.epi.ldc = D;
+    for (int r = 0; r < T; ++r) {
+        g2.A[r] = H[r];
+        g2.B[r] = dY;
+        g2.epi.C[r] = dW2[r];
+    }
+    TPMLP_TRY(run_gemm(dt, g2, s));
+
+    // 3. dW1^(r) = X^T dZ^(r): A(m, k) = X[k, m] (MN-major), B(k, n) = dZ^(r)[k, n]
+    GemmProblem g3 = problem((int)D, Fs, (int)N, T, 0, D, 1, Fs, 1, "bwd_dw1_gemm");
+    g3.epi.kind = EPI_STORE;
+    g3.epi.out_f32 = f32;
+    g3.epi.ldc = Fs;
+    for (int r = 0; r < T; ++r) {
+        g3.A[r] = X;
+        g3.B[r] = dZ[r];
+        g3.epi.C[r] = dW1[r];
+    }
+    TPMLP_TRY(run_gemm(dt, g3, s));
+
+    // 4. dX = sum_r dZ^(r) W1^(r)^T: A = dZ^(r) (K-major), B(k, n) = W1^(r)[n, k] (K-major)
+    if (mode == TPMLP_REDUCE_PARTIALS) {
+        const size_t pstride = round256((size_t)N * D * 4);
+        char* pbase = static_cast<char*>(workspace) + T * dz_stride;
+        const float* parts[kMaxG];
+        GemmProblem g4 = problem((int)N, (int)D, Fs, T, 0, Fs, 0, Fs, 0, "bwd_dx_gemm_partials");
+        g4.epi.kind = EPI_STORE;
+        g4.epi.out_f32 = 1;
+        g4.epi.ldc = D;
+        for (int r = 0; r < T; ++r) {
+            float* pr = reinterpret_cast<float*>(pbase + r * pstride);
+            g4.A[r] = dZ[r];
+            g4.B[r] = W1[r];
+            g4.epi.C[r] = pr;
+            parts[r] = pr;
+        }
+        TPMLP_TRY(run_gemm(dt, g4, s));
+        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, nullptr, dX, s, "block_reduce_dx"));
+    } else {
+        GemmProblem g4 = problem((int)N, (int)D, Fs, T, 1, Fs, 0, Fs, 0, "bwd_dx_gemm_splitk");
+        g4.epi.kind = EPI_STORE;
+        g4.epi.out_f32 = f32;
+        g4.epi.ldc = D;
+        g4.epi.C[0] = dX;
+        for (int r = 0; r < T; ++r) {
+            g4.A[r] = dZ[r];
+            g4.B[r] = W1[r];
+        }
+        TPMLP_TRY(run_gemm(dt, g4, s));
+    }
+
+    // 5. bias gradients
+    if (db1 != nullptr)
+        TPMLP_TRY(run_colsum(f32, N, Fs, Fs, T, reinterpret_cast<const void* const*>(dZ), db1, s));
+    if (db2 != nullptr) {
+        const void* in[1] = {dY};
+        void* out[1] = {db2};
+        TPMLP_TRY(run_colsum(f32, N, D, D, 1, in, out, s));
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_block_reduce(tpmlp_dtype dt, int64_t N, int64_t D, int T,
+                                const float* const* partials, const void* b2, void* Y,
+                                void* stream) {
+    if (dt != TPMLP_F32 && dt != TPMLP_BF16) return TPMLP_ERR_DTYPE;
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (D <= 0 || T < 1 || T > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;
+    if (partials == nullptr || Y == nullptr) return TPMLP_ERR_ARG;
+    for (int r = 0; r < T; ++r)
+        if (partials[r] == nullptr) return TPMLP_ERR_ARG;
+    return run_block_reduce(dt == TPMLP_F32, N, D, T, partials, b2, Y,
+                            static_cast<cudaStream_t>(stream), "block_reduce_bias");
+}
+
+tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
+                            const int64_t* targets, float* loss_per_token, float* loss_mean,
+                            int32_t* argmax, int32_t* target_owner, void* stream) {
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (V <= 0 || T < 1 || T > TPMLP_MAX_SHARDS || V % T != 0) return TPMLP_ERR_SHAPE;
+    if (N > 0 && (logits == nullptr || targets == nullptr || loss_per_token == nullptr))
+        return TPMLP_ERR_ARG;
+    if (V > 0x7fffffffLL || N > 0x7fffffffLL) return TPMLP_ERR_SHAPE;
+    return run_vocab_ce(N, V, T, logits, targets, loss_per_token, loss_mean, argmax, target_owner,
+                        static_cast<cudaStream_t>(stream));
+}
+
+const char* tpmlp_status_str(tpmlp_status s) {
+    switch (s) {
+        case TPMLP_OK: return "TPMLP_OK";
+        case TPMLP_ERR_ARG: return "TPMLP_ERR_ARG: invalid argument";
+        case TPMLP_ERR_SHAPE: return "TPMLP_ERR_SHAPE: invalid shape (F % T, V % T, T range, zero width)";
+        case TPMLP_ERR_ALIGN: return "TPMLP_ERR_ALIGN: pointer or row pitch not 16-byte aligned";
+        case TPMLP_ERR_DTYPE: return "TPMLP_ERR_DTYPE: unknown element type";
+        case TPMLP_ERR_CUDA: return "TPMLP_ERR_CUDA: CUDA call failed";
+        case TPMLP_ERR_TIMEOUT: return "TPMLP_ERR_TIMEOUT: a bounded device wait expired";
+        case TPMLP_ERR_WORKSPACE: return "TPMLP_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "unknown tpmlp status";
+}
+
+tpmlp_status tpmlp_check_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TPMLP_ERR_CUDA;
+    int* p = device_error_word();
+    if (p == nullptr) return TPMLP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TPMLP_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TPMLP_ERR_CUDA;
+    return static_cast<tpmlp_status>(v);
+}
+
+void tpmlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1); }
+
+tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    return run_selftest_wait(timeout_ns, static_cast<cudaStream_t>(stream));
+}
+
+int64_t tpmlp_launch_count(void) { return g_launches.load(); }
+
+void tpmlp_timing_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_t_mu);
+    g_timing = on != 0;
+}
+
+int tpmlp_timing_read(tpmlp_kernel_timing* out, int max_entries) {
+    std::lock_guard<std::mutex> lk(g_t_mu);
+    int rc = 0;
+    for (auto& r : g_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            rc = -1;
+        TimingAgg& a = g_agg[r.name];
+        a.launches += 1;
+        a.ms += ms;
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_pending.clear();
+    if (rc < 0) return -1;
+    int n = 0;
+    for (auto& kv : g_agg) {
+        if (n >= max_entries || out == nullptr) break;
+        memset(&out[n], 0, sizeof(out[n]));
+        strncpy(out[n].name, kv.first.c_str(), sizeof(out[n].name) - 1);
+        out[n].launches = kv.second.launches;
+        out[n].total_ms = kv.second.ms;
+        ++n;
+    }
+    return n;
+}
+
+void tpmlp_timing_reset(void) {
+    std::lock_guard<std::mutex> lk(g_t_mu);
+    for (auto& r : g_pending) {
+        cudaEventSynchronize(r.stop);
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_pending.clear();
+    g_agg.clear();
+}
+
+}  // extern "C"

@@ -1,0 +1,132 @@
+// fp32 grouped / shard-folded GEMM on CUDA cores: the exact-fp32 mode of the
+// block (fmaf in fp32, no TF32 tensor cores, whose 10-bit mantissa would not
+// meet a 1e-5 relative bound). 64 x 64 output tile per CTA, 256 threads,
+// 4 x 4 outputs per thread, K staged through shared memory 16 at a time.
+// Same problem description and epilogue semantics as the tensor-core GEMM.
+#include "act.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16;
+
+struct SimtParams {
+    const float* A[kMaxG];
+    const float* B[kMaxG];
+    int64_t lda, ldb;
+    int M, N, K, G, fold;
+    EpiArgs epi;
+};
+
+__device__ __forceinline__ void epi_scalar(const EpiArgs& e, int g, int m, int n, float v) {
+    if (e.bias[g] != nullptr) v += static_cast<const float*>(e.bias[g])[n];
+    if (e.kind == EPI_ACT) {
+        if (e.aux[g] != nullptr) static_cast<float*>(e.aux[g])[(int64_t)m * e.ldaux + n] = v;
+        v = act_fwd(e.act, v);
+    } else if (e.kind == EPI_DACT) {
+        v *= act_grad(e.act, static_cast<const float*>(e.aux[g])[(int64_t)m * e.ldaux + n]);
+    }
+    static_cast<float*>(e.C[g])[(int64_t)m * e.ldc + n] = v;
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
+    __shared__ float As[TK][TM + 4];
+    __shared__ float Bs[TK][TN + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int n0 = blockIdx.x * TN, m0 = blockIdx.y * TM;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    const int ngroups = p.fold ? p.G : 1;
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int g = p.fold ? gi : (int)blockIdx.z;
+        const float* A = p.A[g];
+        const float* B = p.B[g];
+        for (int k0 = 0; k0 < p.K; k0 += TK) {
+            for (int i = threadIdx.x; i < TM * TK; i += 256) {
+                const int mm = A_MN ? i % TM : i / TK;
+                const int kk = A_MN ? i / TM : i % TK;
+                const int m = m0 + mm, k = k0 + kk;
+                float v = 0.f;
+                if (m < p.M && k < p.K)
+                    v = A_MN ? A[(int64_t)k * p.lda + m] : A[(int64_t)m * p.lda + k];
+                As[kk][mm] = v;
+            }
+            for (int i = threadIdx.x; i < TN * TK; i += 256) {
+                const int nn = B_MN ? i % TN : i / TK;
+                const int kk = B_MN ? i / TN : i % TK;
+                const int n = n0 + nn, k = k0 + kk;
+                float v = 0.f;
+                if (n < p.N && k < p.K)
+                    v = B_MN ? B[(int64_t)k * p.ldb + n] : B[(int64_t)n * p.ldb + k];
+                Bs[kk][nn] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < TK; ++kk) {
+                float a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+    }
+    const int g_out = p.fold ? 0 : (int)blockIdx.z;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty + 16 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx + 16 * j;
+            if (m < p.M && n < p.N) epi_scalar(p.epi, g_out, m, n, acc[i][j]);
+        }
+    }
+}
+
+}  // namespace
+
+tpmlp_status run_gemm_simt(const GemmProblem& pr, cudaStream_t s) {
+    if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
+    if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
+    SimtParams kp{};
+    for (int g = 0; g < pr.G; ++g) {
+        kp.A[g] = static_cast<const float*>(pr.A[g]);
+        kp.B[g] = static_cast<const float*>(pr.B[g]);
+    }
+    kp.lda = pr.lda;
+    kp.ldb = pr.ldb;
+    kp.M = pr.M;
+    kp.N = pr.N;
+    kp.K = pr.K;
+    kp.G = pr.G;
+    kp.fold = pr.fold;
+    kp.epi = pr.epi;
+    const unsigned gy = (unsigned)((pr.M + TM - 1) / TM);
+    if (gy > 65535u) return TPMLP_ERR_SHAPE;
+    dim3 grid((pr.N + TN - 1) / TN, gy, pr.fold ? 1 : pr.G);
+    {
+        LaunchScope ls(pr.name, s);
+        if (pr.a_mn && pr.b_mn)
+            simt_gemm_kernel<true, true><<<grid, 256, 0, s>>>(kp);
+        else if (pr.a_mn)
+            simt_gemm_kernel<true, false><<<grid, 256, 0, s>>>(kp);
+        else if (pr.b_mn)
+            simt_gemm_kernel<false, true><<<grid, 256, 0, s>>>(kp);
+        else
+            simt_gemm_kernel<false, false><<<grid, 256, 0, s>>>(kp);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,506 @@
+// Grouped / shard-folded bf16 GEMM on the 5th-generation tensor cores.
+//
+// One persistent CTA per SM, 6 warps with fixed roles:
+//   warp 0      TMA producer: streams A and B k-blocks into a STAGES-deep
+//               shared-memory ring (128-byte swizzled boxes), one mbarrier
+//               pair (full / empty) per stage;
+//   warp 1      tensor-memory owner and MMA issuer: one thread issues
+//               tcgen05.mma (M = 128, N = BN, K = 16) into a TMEM accumulator
+//               and releases each stage with tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane = output row),
+//               fused bias / activation / activation-derivative, global stores.
+// Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap
+// the main loop of tile i + 1.
+//
+// The problem is a batch of G same-shape GEMMs (one per shard r: the column
+// GEMM X W1^(r), the row GEMM H^(r) W2^(r), and the backward products) or,
+// with `fold`, ONE output whose K loop runs over (r, k): the row GEMM's shard
+// sum Y = sum_r H^(r) W2^(r) then happens inside the fp32 accumulator (the
+// block-end reduction of page "一层 MLP 太宽而放不下时怎样切？", §04, done
+// without writing partial sums).
+//
+// Every mbarrier wait is bounded in time (%globaltimer); a wait that runs out
+// records TPMLP_ERR_TIMEOUT, raises a CTA-wide abort flag, and every role
+// leaves its loop. The producer then waits for its own loads in flight, the
+// MMA thread for its own MMAs, and the TMEM owner frees the accumulator.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "act.cuh"
+#include "ptx.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int BM = 128;           // MMA M (rows of A / TMEM lanes)
+constexpr int BK = 64;            // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;        // K of one kind::f16 MMA
+constexpr int NUM_THREADS = 192;
+constexpr int ACC_BUFS = 2;
+constexpr int BOX_MN = 64;        // MN extent of an MN-major box (128 bytes)
+constexpr int MN_BOX_BYTES = BOX_MN * BK * 2;   // 8 KB
+constexpr int GROUP_M = 8;        // raster band height, in M tiles
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+    static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+};
+
+struct TcParams {
+    CUtensorMap tmA[kMaxG];
+    CUtensorMap tmB[kMaxG];
+    int M, N, K;
+    int G, fold;
+    int a_mn, b_mn;
+    int m_tiles, n_tiles, k_blocks;
+    int num_tiles;
+    EpiArgs epi;
+    int* err;
+    uint64_t timeout_ns;
+};
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
+// address, leading- and stride-dimension byte offsets in 16-byte units,
+// descriptor version 1 at bit 46, swizzle mode 2 at bit 61).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
+// A and B (bits 7-9, 10-12 = 1), operand majorness (bits 15, 16: 1 = MN-major),
+// N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int BN>
+__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& m0, int& n0) {
+    const int per_group = p.m_tiles * p.n_tiles;
+    g = p.fold ? 0 : t / per_group;
+    const int local = t - g * per_group;
+    const int band = local / (GROUP_M * p.n_tiles);
+    const int first_m = band * GROUP_M;
+    const int band_m = min(p.m_tiles - first_m, GROUP_M);
+    const int in_band = local - band * GROUP_M * p.n_tiles;
+    m0 = (first_m + in_band % band_m) * BM;
+    n0 = (in_band / band_m) * BN;
+}
+
+// Epilogue of one thread: 32 consecutive columns [col0, col0 + 32) of output
+// row `row`, accumulator values in r[].
+__device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row, int col0, int M,
+                                               int N, const uint32_t (&r)[32]) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    const bool full = (col0 + 32 <= N);
+    if (e.bias[g] != nullptr) {
+        const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(e.bias[g]) + col0;
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(b) + q);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float lo, hi;
+                    unpack_bf16x2(ws[h], lo, hi);
+                    v[q * 8 + 2 * h] += lo;
+                    v[q * 8 + 2 * h + 1] += hi;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N) v[j] += bf2f(b[j]);
+        }
+    }
+    if (row >= M) return;
+    if (e.kind == EPI_ACT) {
+        if (e.aux[g] != nullptr) {
+            __nv_bfloat16* z = static_cast<__nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
+            if (full) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+                    w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+                    w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+                    w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+                    reinterpret_cast<uint4*>(z)[q] = w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < N) z[j] = __float2bfloat16_rn(v[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = act_fwd(e.act, v[j]);
+    } else if (e.kind == EPI_DACT) {
+        const __nv_bfloat16* z =
+            static_cast<const __nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = *(reinterpret_cast<const uint4*>(z) + q);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float lo, hi;
+                    unpack_bf16x2(ws[h], lo, hi);
+                    v[q * 8 + 2 * h] *= act_grad(e.act, lo);
+                    v[q * 8 + 2 * h + 1] *= act_grad(e.act, hi);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N) v[j] *= act_grad(e.act, bf2f(z[j]));
+        }
+    }
+    if (e.out_f32) {
+        float* c = static_cast<float*>(e.C[g]) + (int64_t)row * e.ldc + col0;
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(c)[q] =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N) c[j] = v[j];
+        }
+    } else {
+        __nv_bfloat16* c = static_cast<__nv_bfloat16*>(e.C[g]) + (int64_t)row * e.ldc + col0;
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+                w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+                w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+                w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+                reinterpret_cast<uint4*>(c)[q] = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N) c[j] = __float2bfloat16_rn(v[j]);
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sA0 = smem_u32(smem);
+    const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar0 = smem_u32(bars);
+    // barrier indices
+    const int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = TFULL + ACC_BUFS,
+              DRAIN = TEMPTY + ACC_BUFS;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar(FULL + s), 1);
+            mbar_init(bar(EMPTY + s), 1);
+        }
+        for (int a = 0; a < ACC_BUFS; ++a) {
+            mbar_init(bar(TFULL + a), 1);
+            mbar_init(bar(TEMPTY + a), 4);
+        }
+        mbar_init(bar(DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < p.G; ++g) {
+            prefetch_tmap(&p.tmA[g]);
+            prefetch_tmap(&p.tmB[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kb_per_group = p.k_blocks;
+    const int kb_total = p.fold ? p.G * kb_per_group : kb_per_group;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int g, m0, n0;
+                decode_tile<BN>(p, t, g, m0, n0);
+                for (int kb = 0; kb < kb_total; ++kb) {
+                    const int gk = p.fold ? kb / kb_per_group : g;
+                    const int k0 = (p.fold ? kb - gk * kb_per_group : kb) * BK;
+                    if (!wait_bounded(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(FULL + s);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t a_dst = sA0 + s * C::A_BYTES;
+                    const uint32_t b_dst = sB0 + s * C::B_BYTES;
+                    if (!p.a_mn) {
+                        tma_load_2d(a_dst, &p.tmA[gk], fb, k0, m0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / BOX_MN; ++j)
+                            tma_load_2d(a_dst + j * MN_BOX_BYTES, &p.tmA[gk], fb, m0 + j * BOX_MN, k0);
+                    }
+                    if (!p.b_mn) {
+                        tma_load_2d(b_dst, &p.tmB[gk], fb, k0, n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / BOX_MN; ++j)
+                            tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.tmB[gk], fb, n0 + j * BOX_MN, k0);
+                    }
+                    ++issued;
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Drain: wait until every load issued into this CTA's shared memory
+            // has landed (the most recent min(issued, STAGES) of them).
+            const uint32_t outstanding = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
+            for (uint32_t i = 0; i < outstanding; ++i) {
+                if (s == 0) {
+                    s = C::STAGES - 1;
+                    ph ^= 1u;
+                } else {
+                    --s;
+                }
+                wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            const uint32_t idesc = instr_desc(BM, BN, p.a_mn, p.b_mn);
+            // operand descriptors: K-major boxes advance 32 bytes per K=16 step,
+            // MN-major boxes advance 16 rows of 128 bytes
+            const uint32_t a_lbo = p.a_mn ? MN_BOX_BYTES : 16;
+            const uint32_t b_lbo = p.b_mn ? MN_BOX_BYTES : 16;
+            const uint32_t a_kstep = p.a_mn ? UMMA_K * 128 : UMMA_K * 2;
+            const uint32_t b_kstep = p.b_mn ? UMMA_K * 128 : UMMA_K * 2;
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                if (!wait_bounded(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kb_total; ++kb) {
+                    if (!wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = sA0 + s * C::A_BYTES;
+                    const uint32_t b_base = sB0 + s * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint64_t ad = smem_desc(a_base + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(b_base + k * b_kstep, b_lbo, 1024);
+                        tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(EMPTY + s));
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar(TFULL + acc));
+                if (++acc == ACC_BUFS) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            tc_commit(bar(DRAIN));
+            wait_bounded(bar(DRAIN), 0, abort_flag, p.err, p.timeout_ns, false);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int g, m0, n0;
+            decode_tile<BN>(p, t, g, m0, n0);
+            // one lane waits; the warp stays converged for the .sync.aligned TMEM loads
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(bar(TFULL + acc), aph, abort_flag, p.err, p.timeout_ns, true);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int row = m0 + quarter * 32 + lane;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            for (int c = 0; c < BN; c += 32) {
+                if (n0 + c >= p.N) break;
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld_32cols(tbase + (uint32_t)c, r);
+                tmem_ld_wait();
+                epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+            if (++acc == ACC_BUFS) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix of `outer` rows x `inner` elements, row pitch `ld`
+// elements, read in boxes of box_inner x box_outer with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
+              int box_inner, int box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
+    using C = Cfg<BN>;
+    static TcParams kp;   // large; filled per call under the lock below
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    memset(&kp, 0, sizeof(kp));
+    const int G = pr.G;
+    for (int g = 0; g < G; ++g) {
+        bool ok = pr.a_mn ? make_map(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BOX_MN, BK)
+                          : make_map(&kp.tmA[g], pr.A[g], pr.K, pr.M, pr.lda, BK, BM);
+        ok = ok && (pr.b_mn ? make_map(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, BOX_MN, BK)
+                            : make_map(&kp.tmB[g], pr.B[g], pr.K, pr.N, pr.ldb, BK, BN));
+        if (!ok) return TPMLP_ERR_CUDA;
+    }
+    kp.M = pr.M;
+    kp.N = pr.N;
+    kp.K = pr.K;
+    kp.G = G;
+    kp.fold = pr.fold;
+    kp.a_mn = pr.a_mn;
+    kp.b_mn = pr.b_mn;
+    kp.m_tiles = (pr.M + BM - 1) / BM;
+    kp.n_tiles = (pr.N + BN - 1) / BN;
+    kp.k_blocks = (pr.K + BK - 1) / BK;
+    kp.num_tiles = (pr.fold ? 1 : G) * kp.m_tiles * kp.n_tiles;
+    kp.epi = pr.epi;
+    kp.err = device_error_word();
+    kp.timeout_ns = wait_timeout_ns();
+    if (kp.err == nullptr) return TPMLP_ERR_CUDA;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES) != cudaSuccess)
+            return TPMLP_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const int sms = device_sm_count();
+    const int grid = kp.num_tiles < sms ? kp.num_tiles : sms;
+    {
+        LaunchScope ls(pr.name, s);
+        tc_gemm_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(kp);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+}  // namespace
+
+tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
+    if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
+    if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
+    if (pr.N <= 128) return launch<128>(pr, s);
+    return launch<256>(pr, s);
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,436 @@
+// HBM-bound kernels of the block and of the vocab-parallel cross-entropy.
+//
+// block_reduce: Y = sum_{r=0}^{T-1} P^(r) + b2 over T full-shape fp32 partial
+//   sums (the single-GPU form of the block-end all-reduce SUM and of the
+//   "bias once" rule, page "一层 MLP 太宽而放不下时怎样切？", §04-§05). 128-bit
+//   streaming loads, 8 outputs per thread per step, shards summed in order
+//   r = 0..T-1 in fp32, then b2, then one rounding to the output type.
+// colsum: bias gradients db1^(r) = sum_n dZ^(r)[n, :], db2 = sum_n dY[n, :].
+// vocab_ce: one CTA per token row. For each vocab shard k (contiguous
+//   columns [k V/T, (k+1) V/T)) every thread keeps an online (max, sum of
+//   exp) pair and the index of its first maximum; warp shuffles and a
+//   shared-memory pass give the shard's (m_k, s_k, argmax_k); the shards are
+//   then combined as m = max_k m_k, S = sum_k s_k exp(m_k - m), and the loss
+//   is m + ln S - z[t] (page "unpurerationalist ... 3.4 TP for Embedding",
+//   LM-head bullets; Megatron TP chapter §7.8). One pass over the logits.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "act.cuh"
+#include "ptx.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+// ---------------------------------------------------------------- reduce --
+
+struct ReduceParams {
+    const float* P[kMaxG];
+    int T;
+    int64_t N, D;
+    const void* bias;
+    void* Y;
+};
+
+template <typename OutT>
+__device__ __forceinline__ float load_out(const void* p, int64_t i) {
+    if constexpr (sizeof(OutT) == 4) {
+        return static_cast<const float*>(p)[i];
+    } else {
+        return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+    }
+}
+
+template <typename OutT, int NT>
+__global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParams p) {
+    const int64_t total8 = p.N * p.D / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total8; i += stride) {
+        float acc[8];
+        {
+            const float4* src = reinterpret_cast<const float4*>(p.P[0]) + 2 * i;
+            const float4 a = __ldcs(src), b = __ldcs(src + 1);
+            acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+            acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+        }
+        constexpr int kLoop = NT > 0 ? NT : kMaxG;
+#pragma unroll
+        for (int r = 1; r < kLoop; ++r) {
+            if (NT == 0 && r >= p.T) break;
+            const float4* src = reinterpret_cast<const float4*>(p.P[r]) + 2 * i;
+            const float4 a = __ldcs(src), b = __ldcs(src + 1);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        if (p.bias != nullptr) {
+            const int64_t col = (8 * i) % p.D;
+            if constexpr (sizeof(OutT) == 4) {
+                const float4* bb = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + col);
+                const float4 a = __ldg(bb), b = __ldg(bb + 1);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            } else {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.bias) + col));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float lo, hi;
+                    unpack_bf16x2(ws[h], lo, hi);
+                    acc[2 * h] += lo;
+                    acc[2 * h + 1] += hi;
+                }
+            }
+        }
+        if constexpr (sizeof(OutT) == 4) {
+            float4* dst = reinterpret_cast<float4*>(p.Y) + 2 * i;
+            __stcs(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            __stcs(dst + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        } else {
+            uint4 w;
+            w.x = pack_bf16x2(acc[0], acc[1]);
+            w.y = pack_bf16x2(acc[2], acc[3]);
+            w.z = pack_bf16x2(acc[4], acc[5]);
+            w.w = pack_bf16x2(acc[6], acc[7]);
+            __stcs(reinterpret_cast<uint4*>(p.Y) + i, w);
+        }
+    }
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(256) block_reduce_scalar_kernel(const ReduceParams p) {
+    const int64_t total = p.N * p.D;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        float acc = p.P[0][i];
+        for (int r = 1; r < p.T; ++r) acc += p.P[r][i];
+        if (p.bias != nullptr) acc += load_out<OutT>(p.bias, i % p.D);
+        if constexpr (sizeof(OutT) == 4) {
+            static_cast<float*>(p.Y)[i] = acc;
+        } else {
+            static_cast<__nv_bfloat16*>(p.Y)[i] = __float2bfloat16_rn(acc);
+        }
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_reduce(const ReduceParams& kp, bool vec, int grid, cudaStream_t s) {
+    if (!vec) {
+        block_reduce_scalar_kernel<OutT><<<grid, 256, 0, s>>>(kp);
+    } else {
+        switch (kp.T) {
+            case 1: block_reduce_vec_kernel<OutT, 1><<<grid, 256, 0, s>>>(kp); break;
+            case 2: block_reduce_vec_kernel<OutT, 2><<<grid, 256, 0, s>>>(kp); break;
+            case 4: block_reduce_vec_kernel<OutT, 4><<<grid, 256, 0, s>>>(kp); break;
+            case 8: block_reduce_vec_kernel<OutT, 8><<<grid, 256, 0, s>>>(kp); break;
+            default: block_reduce_vec_kernel<OutT, 0><<<grid, 256, 0, s>>>(kp); break;
+        }
+    }
+    return cudaGetLastError();
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- colsum --
+
+struct ColsumParams {
+    const void* in[kMaxG];
+    void* out[kMaxG];
+    int64_t rows, cols, ld;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_kernel(const ColsumParams p) {
+    __shared__ float red[8][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = blockIdx.y;
+    const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    float s = 0.f;
+    if (c < p.cols) {
+        const T* in = static_cast<const T*>(p.in[g]);
+        for (int64_t r = warp; r < p.rows; r += 8) {
+            if constexpr (sizeof(T) == 4)
+                s += in[r * p.ld + c];
+            else
+                s += __bfloat162float(in[r * p.ld + c]);
+        }
+    }
+    red[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && c < p.cols) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        if constexpr (sizeof(T) == 4)
+            static_cast<float*>(p.out[g])[c] = t;
+        else
+            static_cast<__nv_bfloat16*>(p.out[g])[c] = __float2bfloat16_rn(t);
+    }
+}
+
+// -------------------------------------------------------------- vocab CE --
+
+constexpr int CE_THREADS = 256;
+constexpr int CE_WARPS = CE_THREADS / 32;
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct CEParams {
+    const float* logits;
+    const int64_t* targets;
+    float* loss;
+    int32_t* argmax;
+    int32_t* owner;
+    int64_t N, V, Vs;
+    int T;
+    int vec;
+    int* err;
+};
+
+// Online (max, sum exp(z - max), first argmax) state of one thread.
+struct LseState {
+    float m;
+    float s;
+    int64_t a;
+};
+
+__device__ __forceinline__ void lse_push(LseState& st, float x, int64_t idx) {
+    if (x > st.m) {
+        st.s = st.s * exp2f((st.m - x) * LOG2E) + 1.f;
+        st.m = x;
+        st.a = idx;
+    } else {
+        st.s += exp2f((x - st.m) * LOG2E);
+    }
+}
+
+// Merge two states: the larger max wins; on equal maxima the lower index.
+__device__ __forceinline__ void lse_merge(LseState& st, float m2, float s2, int64_t a2) {
+    if (m2 == -INFINITY) return;
+    if (st.m == -INFINITY) {
+        st.m = m2; st.s = s2; st.a = a2;
+        return;
+    }
+    const float M = fmaxf(st.m, m2);
+    st.s = st.s * exp2f((st.m - M) * LOG2E) + s2 * exp2f((m2 - M) * LOG2E);
+    if (m2 > st.m || (m2 == st.m && a2 < st.a)) st.a = a2;
+    st.m = M;
+}
+
+__global__ void __launch_bounds__(CE_THREADS) vocab_ce_kernel(const CEParams p) {
+    __shared__ float sm_m[kMaxG][CE_WARPS];
+    __shared__ float sm_s[kMaxG][CE_WARPS];
+    __shared__ long long sm_a[kMaxG][CE_WARPS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = blockIdx.x;
+    const float* z = p.logits + row * p.V;
+
+    for (int k = 0; k < p.T; ++k) {
+        LseState st{-INFINITY, 0.f, 0x7fffffffffffffffLL};
+        const int64_t base = (int64_t)k * p.Vs;
+        if (p.vec) {
+            const float4* zv = reinterpret_cast<const float4*>(z + base);
+            const int64_t n4 = p.Vs / 4;
+            int64_t i = threadIdx.x;
+            // four independent 16-byte loads in flight per thread
+            for (; i + 3 * CE_THREADS < n4; i += 4 * CE_THREADS) {
+                float4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x[u] = __ldcs(zv + i + u * CE_THREADS);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t idx = base + 4 * (i + u * CE_THREADS);
+                    lse_push(st, x[u].x, idx);
+                    lse_push(st, x[u].y, idx + 1);
+                    lse_push(st, x[u].z, idx + 2);
+                    lse_push(st, x[u].w, idx + 3);
+                }
+            }
+            for (; i < n4; i += CE_THREADS) {
+                const float4 x = __ldcs(zv + i);
+                const int64_t idx = base + 4 * i;
+                lse_push(st, x.x, idx);
+                lse_push(st, x.y, idx + 1);
+                lse_push(st, x.z, idx + 2);
+                lse_push(st, x.w, idx + 3);
+            }
+        } else {
+            for (int64_t i = threadIdx.x; i < p.Vs; i += CE_THREADS) lse_push(st, z[base + i], base + i);
+        }
+        // warp combine
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, st.m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, st.s, off);
+            const long long a2 = __shfl_xor_sync(0xffffffffu, (long long)st.a, off);
+            lse_merge(st, m2, s2, a2);
+        }
+        if (lane == 0) {
+            sm_m[k][warp] = st.m;
+            sm_s[k][warp] = st.s;
+            sm_a[k][warp] = st.a;
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // lane k < T combines shard k over the warps of the CTA
+    LseState sh{-INFINITY, 0.f, 0x7fffffffffffffffLL};
+    if (lane < p.T) {
+        for (int w = 0; w < CE_WARPS; ++w) lse_merge(sh, sm_m[lane][w], sm_s[lane][w], sm_a[lane][w]);
+    }
+    // combine the shards: m = max_k m_k, S = sum_k s_k exp(m_k - m)
+    float m = sh.m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float term = (lane < p.T && sh.m != -INFINITY) ? sh.s * exp2f((sh.m - m) * LOG2E) : 0.f;
+    // lowest index among shards whose max equals the global max
+    long long a = (lane < p.T && sh.m == m) ? (long long)sh.a : 0x7fffffffffffffffLL;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        term += __shfl_xor_sync(0xffffffffu, term, off);
+        const long long a2 = __shfl_xor_sync(0xffffffffu, a, off);
+        a = a2 < a ? a2 : a;
+    }
+    if (lane == 0) {
+        const int64_t t = p.targets[row];
+        float loss;
+        if (t < 0 || t >= p.V) {
+            loss = __int_as_float(0x7fc00000);   // NaN
+            atomicCAS(p.err, 0, (int)TPMLP_ERR_ARG);
+            if (p.owner) p.owner[row] = -1;
+        } else {
+            const int64_t own = t / p.Vs;
+            // the owning shard reads its local logit t - own * Vs
+            const float zt = z[own * p.Vs + (t - own * p.Vs)];
+            loss = m + logf(term) - zt;
+            if (p.owner) p.owner[row] = (int32_t)own;
+        }
+        p.loss[row] = loss;
+        if (p.argmax) p.argmax[row] = (int32_t)a;
+    }
+}
+
+// mean of the per-token losses, one CTA, fixed summation order, fp64 accumulator
+__global__ void __launch_bounds__(1024) mean_kernel(const float* loss, int64_t N, float* out) {
+    __shared__ double red[1024];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < N; i += 1024) s += (double)loss[i];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 512; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *out = N > 0 ? (float)(red[0] / (double)N) : __int_as_float(0x7fc00000);
+}
+
+// ------------------------------------------------------------- self test --
+
+__global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing arrives on this barrier: the bounded wait has to run out
+        wait_bounded(smem_u32(&bar), 0, &abort_flag, err, timeout_ns, true);
+    }
+}
+
+}  // namespace
+
+tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const float* const* P,
+                              const void* bias, void* Y, cudaStream_t s, const char* name) {
+    if (N == 0) return TPMLP_OK;
+    ReduceParams kp{};
+    bool vec = (D % 8 == 0) && aligned16(Y) && (bias == nullptr || aligned16(bias));
+    for (int r = 0; r < T; ++r) {
+        kp.P[r] = P[r];
+        vec = vec && aligned16(P[r]);
+    }
+    kp.T = T;
+    kp.N = N;
+    kp.D = D;
+    kp.bias = bias;
+    kp.Y = Y;
+    const int64_t work = vec ? N * D / 8 : N * D;
+    const int64_t max_grid = (int64_t)device_sm_count() * 8;
+    int64_t grid = (work + 255) / 256;
+    if (grid > max_grid) grid = max_grid;
+    if (grid < 1) grid = 1;
+    cudaError_t e;
+    {
+        LaunchScope ls(name, s);
+        e = out_f32 ? launch_reduce<float>(kp, vec, (int)grid, s)
+                    : launch_reduce<__nv_bfloat16>(kp, vec, (int)grid, s);
+    }
+    return e == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status run_colsum(int f32, int64_t rows, int64_t cols, int64_t ld, int G,
+                        const void* const* in, void* const* out, cudaStream_t s) {
+    if (cols == 0 || G == 0) return TPMLP_OK;
+    ColsumParams kp{};
+    for (int g = 0; g < G; ++g) {
+        kp.in[g] = in[g];
+        kp.out[g] = out[g];
+    }
+    kp.rows = rows;
+    kp.cols = cols;
+    kp.ld = ld;
+    dim3 grid((unsigned)((cols + 31) / 32), (unsigned)G);
+    {
+        LaunchScope ls("bias_grad_colsum", s);
+        if (f32)
+            colsum_kernel<float><<<grid, 256, 0, s>>>(kp);
+        else
+            colsum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(kp);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
+                          const int64_t* targets, float* loss, float* loss_mean, int32_t* argmax,
+                          int32_t* owner, cudaStream_t s) {
+    if (N > 0) {
+        CEParams kp{};
+        kp.logits = logits;
+        kp.targets = targets;
+        kp.loss = loss;
+        kp.argmax = argmax;
+        kp.owner = owner;
+        kp.N = N;
+        kp.V = V;
+        kp.Vs = V / T;
+        kp.T = T;
+        kp.vec = (kp.Vs % 4 == 0) && aligned16(logits);
+        kp.err = device_error_word();
+        if (kp.err == nullptr) return TPMLP_ERR_CUDA;
+        if (N > 0x7fffffffLL) return TPMLP_ERR_SHAPE;
+        LaunchScope ls("vocab_ce_fwd", s);
+        vocab_ce_kernel<<<(unsigned)N, CE_THREADS, 0, s>>>(kp);
+    }
+    if (cudaGetLastError() != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (loss_mean != nullptr) {
+        LaunchScope ls("vocab_ce_mean", s);
+        mean_kernel<<<1, 1024, 0, s>>>(loss, N, loss_mean);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status run_selftest_wait(uint64_t timeout_ns, cudaStream_t s) {
+    int* err = device_error_word();
+    if (err == nullptr) return TPMLP_ERR_CUDA;
+    {
+        LaunchScope ls("selftest_wait", s);
+        selftest_wait_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+}  // namespace tpmlp

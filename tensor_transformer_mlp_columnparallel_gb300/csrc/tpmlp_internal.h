@@ -1,0 +1,87 @@
+// Host-side interfaces shared by the library's translation units (not part of
+// the public C-ABI in include/tpmlp.h).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "tpmlp.h"
+
+namespace tpmlp {
+
+constexpr int kMaxG = TPMLP_MAX_SHARDS;
+
+// What the GEMM epilogue does with each fp32 accumulator value v at (m, n):
+//   EPI_STORE: C = v (+ bias[n])
+//   EPI_ACT:   z = v (+ bias[n]); aux = z (if aux != NULL); C = act(z)
+//   EPI_DACT:  C = v * act'(aux[m, n])
+enum EpiKind { EPI_STORE = 0, EPI_ACT = 1, EPI_DACT = 2 };
+
+struct EpiArgs {
+    int kind;
+    int act;                   // tpmlp_act
+    int out_f32;               // 1: C is fp32; 0: C has the compute element type
+    int64_t ldc;               // row pitch of C, elements
+    int64_t ldaux;             // row pitch of aux, elements
+    void* C[kMaxG];            // per group (FOLD: group 0 only)
+    const void* bias[kMaxG];   // per output column, compute element type; NULL: none
+    void* aux[kMaxG];          // Z (compute element type), see EpiKind
+};
+
+// A batch of G GEMMs of identical shape, C_g[M, N] = A_g[M, K] B_g[K, N], or,
+// with fold = 1, ONE output C[M, N] = sum_g A_g B_g whose K loop runs over
+// (g, k) in order g = 0..G-1.
+// Operand addressing (elements):
+//   A(m, k) = a_mn ? A[g][k * lda + m] : A[g][m * lda + k]
+//   B(k, n) = b_mn ? B[g][k * ldb + n] : B[g][n * ldb + k]
+// ("K-major" = the K index is contiguous; "MN-major" = M or N is contiguous.)
+struct GemmProblem {
+    int M, N, K;
+    int G;
+    int fold;
+    const void* A[kMaxG];
+    int64_t lda;
+    int a_mn;
+    const void* B[kMaxG];
+    int64_t ldb;
+    int b_mn;
+    EpiArgs epi;
+    const char* name;          // kernel kind, for the timing records
+};
+
+// bf16 inputs on tcgen05 tensor cores (TMA + mbarrier pipeline + TMEM).
+tpmlp_status run_gemm_tc(const GemmProblem& p, cudaStream_t s);
+// fp32 inputs on CUDA cores (exact fp32 FMA, no TF32).
+tpmlp_status run_gemm_simt(const GemmProblem& p, cudaStream_t s);
+
+// Y = sum_r P[r] + bias, fp32 sum in shard order, output fp32 or bf16.
+tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const float* const* P,
+                              const void* bias, void* Y, cudaStream_t s, const char* name);
+// out_g[c] = sum_r in_g[r * ld + c] for G groups (bias gradients).
+tpmlp_status run_colsum(int f32, int64_t rows, int64_t cols, int64_t ld, int G,
+                        const void* const* in, void* const* out, cudaStream_t s);
+tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
+                          const int64_t* targets, float* loss, float* loss_mean, int32_t* argmax,
+                          int32_t* owner, cudaStream_t s);
+tpmlp_status run_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
+
+// ---- services of the API translation unit --------------------------------
+int* device_error_word();          // per current device; NULL on failure
+uint64_t wait_timeout_ns();
+int device_sm_count();
+
+// Counts the launch and, when timing is on, brackets it with CUDA events
+// recorded on the launch stream.
+class LaunchScope {
+  public:
+    LaunchScope(const char* name, cudaStream_t s);
+    ~LaunchScope();
+
+  private:
+    const char* name_;
+    cudaStream_t s_;
+    cudaEvent_t start_;
+    cudaEvent_t stop_;
+};
+
+}  // namespace tpmlp

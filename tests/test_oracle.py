@@ -152,6 +152,14 @@ def test_bias_added_per_shard_gives_y_plus_t_b2_and_is_detected(T):
     assert normwise_rel_err(wrong, right) > TOL["bf16"]
 
 
+def test_block_reduce_worked_example_and_bias_once():
+    g = load("worked_example.json")
+    parts = [arr(p) for p in g["expected"]["partials"]]
+    np.testing.assert_array_equal(osh.block_reduce(parts, None), arr(g["expected"]["Y"]))
+    b2 = np.array([0.5, -2.0])
+    np.testing.assert_array_equal(osh.block_reduce(parts, b2), arr(g["expected"]["Y"]) + b2)
+
+
 @pytest.mark.parametrize("kind", ["relu", "gelu_tanh"])
 def test_row_first_split_is_wrong(kind):
     rng = np.random.default_rng(0)
