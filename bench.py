@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark of the sharded MLP block's forward + backward on one GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  forward:  column GEMM + bias + GELU-tanh (all T shards), row GEMM with the
+            shard sum folded into the split-K accumulator (b2 once);
+  backward: dZ GEMM with the act' epilogue, dW2 GEMM, dW1 GEMM, dX GEMM with
+            the shard sum folded into split-K.
+Workload: N = 8192 tokens (B=4, L=2048), D = 8192, F = 28672, T = 8, bf16
+storage, fp32 accumulation, no bias, seeded synthetic inputs (X, dY ~ N(0,1),
+W ~ N(0, 0.02)).
+
+The JSON line also carries: the dominant kernel's roofline (CUDA-event
+durations measured live during the timed region), the float64 CPU oracle timed
+on a bounded sample of the same workload, an end-to-end number through the
+public API with host buffers, SM clocks sampled during the timed region, and
+secondary measurements (the PARTIALS variant with its block-end reduce
+kernel, and the vocab-parallel cross-entropy kernel).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads.configs import MLP_CONFIGS, CE_CONFIGS  # noqa: E402
+from workloads.gen import gen_mlp_inputs  # noqa: E402
+
+WORKLOAD = "mlp_bf16_gelu_n8192_d8192_f28672_t8_fwdbwd"
+METRIC = "sharded-MLP fwd+bwd TFLOP/s (% BF16 peak); reduce & CE HBM GB/s (% peak)"
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["splitk", "partials"], default="splitk")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r["power"] is not None and r["power"] > 300] or rows
+        reasons = set()
+        for r in load:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": float(np.median([r["sm"] for r in load])),
+                "sm_max_mhz": float(max(r["max"] for r in rows)),
+                "samples": len(rows), "samples_under_load": len(load),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Block:
+    """Device-resident inputs, outputs and workspace of one fwd+bwd step."""
+
+    def __init__(self, cfg, mode, dev):
+        import tensor_transformer_mlp_columnparallel_gb300 as tp
+        self.tp = tp
+        self.cfg, self.mode, self.dev = cfg, mode, dev
+        inp = gen_mlp_inputs(cfg)
+        self.host = inp
+        self.X = inp.X.to(dev)
+        self.dY = inp.dY.to(dev)
+        self.W1 = [w.to(dev) for w in inp.W1_shards()]
+        self.W2 = [w.contiguous().to(dev) for w in inp.W2_shards()]
+        N, D, Fs, T = cfg.N, cfg.D, cfg.Fs, cfg.T
+        dt = self.X.dtype
+        e = lambda *s: torch.empty(s, dtype=dt, device=dev)
+        self.Y = e(N, D)
+        self.H = [e(N, Fs) for _ in range(T)]
+        self.Z = [e(N, Fs) for _ in range(T)]
+        self.dX = e(N, D)
+        self.dW1 = [e(D, Fs) for _ in range(T)]
+        self.dW2 = [e(Fs, D) for _ in range(T)]
+        wf = tp.tpmlp_workspace_bytes(0, dt, N, D, cfg.F, T, mode)
+        wb = tp.tpmlp_workspace_bytes(1, dt, N, D, cfg.F, T, mode)
+        self.ws = torch.empty(max(wf, wb, 256), dtype=torch.uint8, device=dev)
+
+    def step(self):
+        tp = self.tp
+        tp.tpmlp_forward(self.X, self.W1, None, self.W2, None, self.Y, self.H, self.Z,
+                         self.cfg.act, self.mode, self.ws)
+        tp.tpmlp_backward(self.X, self.W1, self.W2, self.H, self.Z, self.dY, self.dX, self.dW1,
+                          self.dW2, None, None, self.cfg.act, self.mode, self.ws)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed(fn, steps, warmup, world, dev, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return a.elapsed_time(b)
+
+
+def kernel_table(t, total_ms):
+    out = {}
+    for name, v in sorted(t.items(), key=lambda kv: -kv[1]["total_ms"]):
+        out[name] = {"launches": v["launches"], "ms_per_launch": v["total_ms"] / max(v["launches"], 1),
+                     "share": v["total_ms"] / total_ms if total_ms > 0 else None}
+    return out
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    it is for the current build of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        return d.get(kernel, {}).get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def cpu_baseline_mlp(cfg, tokens=96):
+    """Float64 oracle fwd+bwd on `tokens` rows of the same workload, all
+    host cores (numpy / OpenBLAS default threading). The per-token work of
+    fwd+bwd is 12 D F FLOP (two forward GEMM rows, four backward)."""
+    import oracle
+    inp = gen_mlp_inputs(cfg, N=tokens)
+    W1 = oracle.mlp.as_f64(inp.W1)
+    W2 = oracle.mlp.as_f64(inp.W2)
+    t0 = time.perf_counter()
+    oracle.mlp.forward(inp.X, W1, None, W2, None, cfg.act)
+    oracle.mlp.backward(inp.X, W1, None, W2, inp.dY, cfg.act)
+    dt = time.perf_counter() - t0
+    flops = 12.0 * tokens * cfg.D * cfg.F
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} of {cfg.N} tokens, fwd+bwd, float64 numpy (OpenBLAS threads = "
+                      f"host cores), {dt:.1f} s"}
+
+
+def secondary(dev, stream, steps, pk):
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+    out = {}
+    # vocab-parallel CE, N = 8192, V = 128000, T = 8: logits drawn on the device
+    ce = CE_CONFIGS["vocab_ce_n8192_v128000_t8"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    logits = torch.randn((ce.N, ce.V), generator=g, device=dev) * ce.logit_std
+    targets = torch.randint(0, ce.V, (ce.N,), generator=g, device=dev)
+    loss = torch.empty(ce.N, device=dev)
+    mean = torch.empty(1, device=dev)
+    amax = torch.empty(ce.N, dtype=torch.int32, device=dev)
+    own = torch.empty(ce.N, dtype=torch.int32, device=dev)
+    fn = lambda: tp.tpmlp_vocab_ce(logits, targets, ce.T, loss, mean, amax, own)
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    timed(fn, steps, 3, 1, dev, stream)
+    tp.tpmlp_timing_enable(False)
+    t = tp.tpmlp_timing_read()
+    k = t["vocab_ce_fwd"]
+    ms = k["total_ms"] / k["launches"]
+    gbs = ce.algorithmic_bytes() / (ms * 1e-3) / 1e9
+    out["vocab_ce_n8192_v128000_t8"] = {
+        "kernel": "vocab_ce_fwd", "ms_per_launch": ms, "GB/s": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": load_traffic("vocab_ce_fwd")}}
+    del logits
+    torch.cuda.empty_cache()
+    # the PARTIALS variant of the same fwd+bwd step: T fp32 partials + block reduce
+    cfg = MLP_CONFIGS[WORKLOAD]
+    blk = Block(cfg, "partials", dev)
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    ms_total = timed(blk.step, max(3, steps // 2), 3, 1, dev, stream)
+    tp.tpmlp_timing_enable(False)
+    t = tp.tpmlp_timing_read()
+    nsteps = max(3, steps // 2)
+    flops = (cfg.fwd_flops() + cfg.bwd_flops()) * nsteps
+    red_bytes = cfg.T * cfg.N * cfg.D * 4 + cfg.N * cfg.D * 2   # read T fp32 partials, write bf16
+    rk = {}
+    for name in ("block_reduce_bias", "block_reduce_dx"):
+        if name in t:
+            ms = t[name]["total_ms"] / t[name]["launches"]
+            gbs = red_bytes / (ms * 1e-3) / 1e9
+            rk[name] = {"ms_per_launch": ms, "GB/s": gbs,
+                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                                     "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                                     "traffic": load_traffic(name)}}
+    out["partials_variant_" + WORKLOAD] = {
+        "TFLOP/s": flops / (ms_total * 1e-3) / 1e12, "ms_per_step": ms_total / nsteps,
+        "reduce_kernels": rk, "kernels": kernel_table(t, ms_total)}
+    return out
+
+
+def e2e_measure(blk, steps, stream):
+    """The same step through the public API with host buffers: pinned host
+    inputs copied in, outputs copied back, every step, inside the timed region."""
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+    h = blk.host
+    pin = lambda t: t.contiguous().pin_memory()
+    hX, hdY = pin(h.X), pin(h.dY)
+    hW1 = [pin(w) for w in h.W1_shards()]
+    hW2 = [pin(w) for w in h.W2_shards()]
+    oY, odX = torch.empty_like(hX).pin_memory(), torch.empty_like(hX).pin_memory()
+    odW1 = [torch.empty_like(w).pin_memory() for w in hW1]
+    odW2 = [torch.empty_like(w).pin_memory() for w in hW2]
+    h2d = sum(t.numel() * t.element_size() for t in [hX, hdY, *hW1, *hW2])
+    d2h = sum(t.numel() * t.element_size() for t in [oY, odX, *odW1, *odW2])
+
+    def step():
+        blk.X.copy_(hX, non_blocking=True)
+        blk.dY.copy_(hdY, non_blocking=True)
+        for d, s in zip(blk.W1, hW1):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(blk.W2, hW2):
+            d.copy_(s, non_blocking=True)
+        blk.step()
+        oY.copy_(blk.Y, non_blocking=True)
+        odX.copy_(blk.dX, non_blocking=True)
+        for d, s in zip(odW1, blk.dW1):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(odW2, blk.dW2):
+            d.copy_(s, non_blocking=True)
+    ms = timed(step, steps, 2, 1, blk.dev, stream)
+    return ms, h2d, d2h
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+
+    cfg = MLP_CONFIGS[WORKLOAD]
+    pk = peaks()
+    blk = Block(cfg, args.mode, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        blk.step()
+    torch.cuda.synchronize()
+    assert tp.tpmlp_check_device_error() == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    launches0 = tp.tpmlp_launch_count()
+    ms = timed(blk.step, args.steps, 0, world, dev, stream)
+    launches = tp.tpmlp_launch_count() - launches0
+    tp.tpmlp_timing_enable(False)
+    clk = clocks.stop()
+    kt = tp.tpmlp_timing_read()
+    status = tp.tpmlp_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error word {status} after the timed region")
+
+    ms_max = max_over_ranks(ms, world, dev)
+    flops_step = cfg.fwd_flops() + cfg.bwd_flops()
+    value = flops_step * args.steps * world / (ms_max * 1e-3) / 1e12
+    ktab = kernel_table(kt, ms)
+    dom = max(kt.items(), key=lambda kv: kv[1]["total_ms"])[0]
+    dom_ms = kt[dom]["total_ms"] / kt[dom]["launches"]
+    gemm_flops = 2.0 * cfg.N * cfg.D * cfg.F      # every GEMM of the step has this size
+    achieved = gemm_flops / (dom_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": load_traffic(dom), "kernel": dom,
+            "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a "
+                           f"back-to-back step loop)",
+            "algorithmic_flops_per_launch": gemm_flops}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; X, dY ~ N(0,1), W ~ N(0,0.02))",
+        "config": {"workload": WORKLOAD, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
+                   "F": cfg.F, "T": cfg.T, "act": cfg.act, "bias": False,
+                   "reduce_mode": args.mode, "pass": "forward+backward",
+                   "l2": "inputs larger than L2 (weights 0.94 GB, activations 1.1 GB per step)",
+                   "parallelism": f"replicas x{world} (T logical shards per GPU)"},
+        "frac_of_peak_step": value / world / peak,
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernels": ktab,
+    }
+    if rank == 0 and not args.no_e2e:
+        e_ms, h2d, d2h = e2e_measure(blk, min(args.steps, 5), stream)
+        n_e = min(args.steps, 5)
+        line["e2e"] = {"value": flops_step * n_e / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e_ms / n_e, "steps": n_e}
+    del blk
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_secondary:
+        line["secondary"] = secondary(dev, stream, args.steps, pk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_mlp(cfg)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cfg = MLP_CONFIGS[WORKLOAD]
+    tokens = 32
+    inp = gen_mlp_inputs(cfg, N=tokens)
+    W1 = oracle.mlp.as_f64(inp.W1)
+    W2 = oracle.mlp.as_f64(inp.W2)
+
+    def step():
+        oracle.mlp.forward(inp.X, W1, None, W2, None, cfg.act)
+        oracle.mlp.backward(inp.X, W1, None, W2, inp.dY, cfg.act)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 12.0 * tokens * cfg.D * cfg.F * args.steps
+    value = flops / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{tokens} of {cfg.N} tokens per step, fwd+bwd, float64 numpy (OpenBLAS threads = "
+              f"host cores)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "N": cfg.N, "D": cfg.D, "F": cfg.F, "T": cfg.T,
+                   "act": cfg.act, "pass": "forward+backward"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
