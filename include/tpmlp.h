@@ -133,6 +133,33 @@ tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
                             const int64_t* targets, float* loss_per_token, float* loss_mean,
                             int32_t* argmax, int32_t* target_owner, void* stream);
 
+/* Size in bytes of the library's own scratch array (see tpmlp_forward_noalloc). */
+#define TPMLP_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* tpmlp_forward in PARTIALS mode for callers that cannot allocate device
+ * memory: the T fp32 partial sums live in a fixed array inside the library
+ * instead of a caller workspace. The pages have no counterpart to this call;
+ * it exists for callers such as a plug-in inside a host program that owns all
+ * device memory, or a latency-bound loop that must not risk a cudaMalloc
+ * (which can fail or synchronise the device).
+ * - It allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * - The array is static device memory of TPMLP_NOALLOC_SCRATCH_BYTES (8 MiB);
+ *   every GPU that loads the library holds it until the process exits.
+ * - Shapes must satisfy T * round_up(N*D*4, 256) <= TPMLP_NOALLOC_SCRATCH_BYTES
+ *   (e.g. T = 8, N = 16, D = 12288); larger ones return TPMLP_ERR_WORKSPACE
+ *   and launch nothing.
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ * - All calls share the one array. Calls whose GPU work can overlap (other
+ *   streams, other host threads without ordering) race on it; calls on one
+ *   stream are ordered. What an earlier call left in it is never read: the
+ *   row GEMM overwrites every partial before the reduce reads it.
+ * Arguments, outputs and the other errors are those of tpmlp_forward. */
+tpmlp_status tpmlp_forward_noalloc(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                   tpmlp_act act, const void* X, const void* const* W1,
+                                   const void* const* b1, const void* const* W2, const void* b2,
+                                   void* Y, void* const* H, void* const* Z, void* stream);
+
 /* Workspace bytes tpmlp_forward / tpmlp_backward need for these arguments
  * (0 for a forward in SPLITK mode). Returns (size_t)-1 for invalid shapes. */
 size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     tpmlp_block_reduce,
     tpmlp_check_device_error,
     tpmlp_forward,
+    tpmlp_forward_noalloc,
     tpmlp_launch_count,
     tpmlp_selftest_wait_timeout,
     tpmlp_set_wait_timeout_ns,

@@ -47,6 +47,8 @@ _PP = ctypes.POINTER(ctypes.c_void_p)
 _SIGNATURES = {
     "tpmlp_forward": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _vp, _vp,
                              _PP, _PP, _int, _vp, ctypes.c_size_t, _vp]),
+    "tpmlp_forward_noalloc": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _vp,
+                                     _vp, _PP, _PP, _vp]),
     "tpmlp_backward": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _PP, _vp,
                               _vp, _PP, _PP, _PP, _vp, _int, _vp, ctypes.c_size_t, _vp]),
     "tpmlp_block_reduce": (_int, [_int, _i64, _i64, _int, _PP, _vp, _vp, _vp]),
@@ -153,6 +155,19 @@ def tpmlp_forward(X, W1, b1, W2, b2, Y, H, Z, act: str, mode: str, workspace=Non
     _check(lib().tpmlp_forward(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X), _ptrs(W1),
                                _ptrs(b1), _ptrs(W2), _ptr(b2), _ptr(Y), _ptrs(H), _ptrs(Z),
                                MODE[mode], _ptr(workspace), ws_bytes, _stream(X)))
+
+
+def tpmlp_forward_noalloc(X, W1, b1, W2, b2, Y, H, Z, act: str):
+    """tpmlp_forward in PARTIALS mode with the partial sums in the library's
+    own fixed scratch array (no workspace, no device allocation); see
+    include/tpmlp.h for its size limit and the sharing rules."""
+    T = len(W1)
+    N, D = X.shape
+    Fs = W1[0].shape[1]
+    _require([X, b2, Y, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, None)
+    _check(lib().tpmlp_forward_noalloc(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X),
+                                       _ptrs(W1), _ptrs(b1), _ptrs(W2), _ptr(b2), _ptr(Y),
+                                       _ptrs(H), _ptrs(Z), _stream(X)))
 
 
 def tpmlp_backward(X, W1, W2, H, Z, dY, dX, dW1, dW2, db1, db2, act: str, mode: str, workspace):

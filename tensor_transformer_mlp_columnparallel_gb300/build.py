@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtpmlp.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "hbm_kernels.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "hbm_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
