@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="N,D,F,T override of the fwd+bwd workload (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -173,6 +175,16 @@ class Block:
                          self.cfg.act, self.mode, self.ws)
         tp.tpmlp_backward(self.X, self.W1, self.W2, self.H, self.Z, self.dY, self.dX, self.dW1,
                           self.dW2, None, None, self.cfg.act, self.mode, self.ws)
+
+
+def workload_config(args):
+    cfg = MLP_CONFIGS[WORKLOAD]
+    if args.shape:
+        import dataclasses
+        N, D, F, T = (int(x) for x in args.shape.split(","))
+        cfg = dataclasses.replace(cfg, name=f"{WORKLOAD}_shape_{N}_{D}_{F}_{T}", B=1, L=N, D=D,
+                                  F=F, T=T)
+    return cfg
 
 
 def barrier(world):
@@ -342,7 +354,7 @@ def run_ours(args):
     __graft_entry__.build()
     import tensor_transformer_mlp_columnparallel_gb300 as tp
 
-    cfg = MLP_CONFIGS[WORKLOAD]
+    cfg = workload_config(args)
     pk = peaks()
     blk = Block(cfg, args.mode, dev)
     stream = torch.cuda.current_stream(dev)
@@ -385,7 +397,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; X, dY ~ N(0,1), W ~ N(0,0.02))",
-        "config": {"workload": WORKLOAD, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
+        "config": {"workload": cfg.name, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
                    "F": cfg.F, "T": cfg.T, "act": cfg.act, "bias": False,
                    "reduce_mode": args.mode, "pass": "forward+backward",
                    "l2": "inputs larger than L2 (weights 0.94 GB, activations 1.1 GB per step)",
@@ -448,7 +460,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "N": cfg.N, "D": cfg.D, "F": cfg.F, "T": cfg.T,
+        "config": {"workload": cfg.name, "N": cfg.N, "D": cfg.D, "F": cfg.F, "T": cfg.T,
                    "act": cfg.act, "pass": "forward+backward"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},

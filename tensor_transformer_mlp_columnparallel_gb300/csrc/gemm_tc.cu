@@ -45,17 +45,24 @@ constexpr int BOX_MN = 64;        // MN extent of an MN-major box (128 bytes)
 constexpr int MN_BOX_BYTES = BOX_MN * BK * 2;   // 8 KB
 constexpr int GROUP_M = 8;        // raster band height, in M tiles
 
-template <int BN>
+// BN: accumulator columns (MMA N). PAIR: a CTA pair (cluster of 2) issues
+// cta_group::2 MMAs of M = 256; each CTA stages its own 128 rows of A and its
+// own BN/2 rows of B, which halves the B bytes each SM pulls from L2.
+template <int BN, bool PAIR>
 struct Cfg {
+    static constexpr int CTAS = PAIR ? 2 : 1;
+    static constexpr int TILE_M = BM * CTAS;
+    static constexpr int B_ROWS = BN / CTAS;                 // B rows (N) staged per CTA
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
+    static constexpr int STAGES = STAGE_BYTES <= 32768 ? 6 : 4;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
     static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+    static_assert(B_ROWS % BOX_MN == 0, "MN-major B boxes");
 };
 
 struct TcParams {
@@ -91,7 +98,7 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& m0, int& n0) {
     const int per_group = p.m_tiles * p.n_tiles;
     g = p.fold ? 0 : t / per_group;
@@ -100,7 +107,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
     const int first_m = band * GROUP_M;
     const int band_m = min(p.m_tiles - first_m, GROUP_M);
     const int in_band = local - band * GROUP_M * p.n_tiles;
-    m0 = (first_m + in_band % band_m) * BM;
+    m0 = (first_m + in_band % band_m) * TILE_M;
     n0 = (in_band / band_m) * BN;
 }
 
@@ -209,9 +216,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
     }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -228,6 +235,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;      // CTA within the pair
+    const bool leader = rank == 0;
+    const int first_tile = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int tile_step = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         }
         for (int a = 0; a < ACC_BUFS; ++a) {
             mbar_init(bar(TFULL + a), 1);
-            mbar_init(bar(TEMPTY + a), 4);
+            mbar_init(bar(TEMPTY + a), 4 * C::CTAS);   // every epilogue warp of the pair
         }
         mbar_init(bar(DRAIN), 1);
         *abort_flag = 0;
@@ -250,11 +261,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // peer barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -263,14 +280,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer (each CTA loads its own rows) ----------------
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
                 int g, m0, n0;
-                decode_tile<BN>(p, t, g, m0, n0);
+                decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
+                const int am0 = m0 + (int)rank * BM;          // this CTA's A rows
+                const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
                 for (int kb = 0; kb < kb_total; ++kb) {
                     const int gk = p.fold ? kb / kb_per_group : g;
                     const int k0 = (p.fold ? kb - gk * kb_per_group : kb) * BK;
@@ -278,23 +297,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar(FULL + s);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    // the pair's stage is complete when BOTH CTAs' bytes landed on the
+                    // even CTA's full barrier
+                    const uint32_t fb = PAIR ? mapa_shared(bar(FULL + s), 0) : bar(FULL + s);
+                    if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
                     const uint32_t a_dst = sA0 + s * C::A_BYTES;
                     const uint32_t b_dst = sB0 + s * C::B_BYTES;
+                    auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+                        if constexpr (PAIR)
+                            tma_load_2d_pair(dst, m, fb, x, y);
+                        else
+                            tma_load_2d(dst, m, fb, x, y);
+                    };
                     if (!p.a_mn) {
-                        tma_load_2d(a_dst, &p.tmA[gk], fb, k0, m0);
+                        load(a_dst, &p.tmA[gk], k0, am0);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / BOX_MN; ++j)
-                            tma_load_2d(a_dst + j * MN_BOX_BYTES, &p.tmA[gk], fb, m0 + j * BOX_MN, k0);
+                            load(a_dst + j * MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
                     }
                     if (!p.b_mn) {
-                        tma_load_2d(b_dst, &p.tmB[gk], fb, k0, n0);
+                        load(b_dst, &p.tmB[gk], k0, bn0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / BOX_MN; ++j)
-                            tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.tmB[gk], fb, n0 + j * BOX_MN, k0);
+                        for (int j = 0; j < C::B_ROWS / BOX_MN; ++j)
+                            load(b_dst + j * MN_BOX_BYTES, &p.tmB[gk], bn0 + j * BOX_MN, k0);
                     }
                     ++issued;
                     if (++s == C::STAGES) {
@@ -303,23 +330,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     }
                 }
             }
-            // Drain: wait until every load issued into this CTA's shared memory
-            // has landed (the most recent min(issued, STAGES) of them).
-            const uint32_t outstanding = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
-            for (uint32_t i = 0; i < outstanding; ++i) {
-                if (s == 0) {
-                    s = C::STAGES - 1;
-                    ph ^= 1u;
-                } else {
-                    --s;
+            // Drain: the even CTA waits until every stage it armed has landed
+            // (its full barriers count the odd CTA's bytes too), so no TMA write
+            // is in flight when the pair leaves (the final cluster barrier holds
+            // the odd CTA until then).
+            if (leader) {
+                const uint32_t outstanding = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
+                for (uint32_t i = 0; i < outstanding; ++i) {
+                    if (s == 0) {
+                        s = C::STAGES - 1;
+                        ph ^= 1u;
+                    } else {
+                        --s;
+                    }
+                    wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, false);
                 }
-                wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, false);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            const uint32_t idesc = instr_desc(BM, BN, p.a_mn, p.b_mn);
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (even CTA of the pair) ----------------
+            const uint32_t idesc = instr_desc(C::TILE_M, BN, p.a_mn, p.b_mn);
             // operand descriptors: K-major boxes advance 32 bytes per K=16 step,
             // MN-major boxes advance 16 rows of 128 bytes
             const uint32_t a_lbo = p.a_mn ? MN_BOX_BYTES : 16;
@@ -331,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
                 if (!wait_bounded(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                     ok = false;
                     break;
@@ -350,40 +381,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint64_t ad = smem_desc(a_base + k * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc(b_base + k * b_kstep, b_lbo, 1024);
-                        tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (PAIR)
+                            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    tc_commit(bar(EMPTY + s));
+                    // frees stage s in both CTAs once these MMAs have read it
+                    if constexpr (PAIR)
+                        tc_commit_pair_multicast(bar(EMPTY + s), 0x3);
+                    else
+                        tc_commit(bar(EMPTY + s));
                     if (++s == C::STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar(TFULL + acc));
+                if constexpr (PAIR)
+                    tc_commit_pair_multicast(bar(TFULL + acc), 0x3);
+                else
+                    tc_commit(bar(TFULL + acc));
                 if (++acc == ACC_BUFS) {
                     acc = 0;
                     aph ^= 1u;
                 }
             }
             // every MMA this thread issued has completed before TMEM is freed
-            tc_commit(bar(DRAIN));
+            if constexpr (PAIR)
+                tc_commit_pair(bar(DRAIN));
+            else
+                tc_commit(bar(DRAIN));
             wait_bounded(bar(DRAIN), 0, abort_flag, p.err, p.timeout_ns, false);
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+        // ---------------- epilogue (warps 2..5 of each CTA) ----------------
         const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
+        // the even CTA's TMEM-empty barrier counts the epilogue warps of both CTAs
+        const uint32_t tempty0 = PAIR ? mapa_shared(bar(TEMPTY), 0) : bar(TEMPTY);
         int acc = 0;
         uint32_t aph = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        for (int t = first_tile; t < p.num_tiles; t += tile_step) {
             int g, m0, n0;
-            decode_tile<BN>(p, t, g, m0, n0);
+            decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
             // one lane waits; the warp stays converged for the .sync.aligned TMEM loads
             int ok = 1;
             if (lane == 0) ok = wait_bounded(bar(TFULL + acc), aph, abort_flag, p.err, p.timeout_ns, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int row = m0 + quarter * 32 + lane;
+            const int row = m0 + (int)rank * BM + quarter * 32 + lane;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             for (int c = 0; c < BN; c += 32) {
@@ -396,7 +442,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+                else
+                    mbar_arrive(bar(TEMPTY + acc));
+            }
             if (++acc == ACC_BUFS) {
                 acc = 0;
                 aph ^= 1u;
@@ -407,8 +458,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the pair's MMAs and loads are done before TMEM is freed
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -445,9 +502,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
     return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     static TcParams kp;   // large; filled per call under the lock below
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
@@ -457,7 +514,7 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
         bool ok = pr.a_mn ? make_map(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BOX_MN, BK)
                           : make_map(&kp.tmA[g], pr.A[g], pr.K, pr.M, pr.lda, BK, BM);
         ok = ok && (pr.b_mn ? make_map(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, BOX_MN, BK)
-                            : make_map(&kp.tmB[g], pr.B[g], pr.K, pr.N, pr.ldb, BK, BN));
+                            : make_map(&kp.tmB[g], pr.B[g], pr.K, pr.N, pr.ldb, BK, C::B_ROWS));
         if (!ok) return TPMLP_ERR_CUDA;
     }
     kp.M = pr.M;
@@ -467,7 +524,7 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
     kp.fold = pr.fold;
     kp.a_mn = pr.a_mn;
     kp.b_mn = pr.b_mn;
-    kp.m_tiles = (pr.M + BM - 1) / BM;
+    kp.m_tiles = (pr.M + C::TILE_M - 1) / C::TILE_M;
     kp.n_tiles = (pr.N + BN - 1) / BN;
     kp.k_blocks = (pr.K + BK - 1) / BK;
     kp.num_tiles = (pr.fold ? 1 : G) * kp.m_tiles * kp.n_tiles;
@@ -477,20 +534,50 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
     if (kp.err == nullptr) return TPMLP_ERR_CUDA;
 
     static bool attr_set[64] = {};
+    static int max_units[64] = {};    // co-resident CTAs (1-CTA) or clusters (pair)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES) != cudaSuccess)
             return TPMLP_ERR_CUDA;
+        int units = device_sm_count();
+        if (PAIR) {
+            cfg.gridDim = dim3(2 * (units / 2));
+            int nclusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, tc_gemm_kernel<BN, PAIR>, &cfg) !=
+                    cudaSuccess ||
+                nclusters < 1)
+                return TPMLP_ERR_CUDA;
+            units = nclusters;
+        }
+        max_units[dev] = units;
         attr_set[dev] = true;
     }
-    const int sms = device_sm_count();
-    const int grid = kp.num_tiles < sms ? kp.num_tiles : sms;
+    const int units = kp.num_tiles < max_units[dev] ? kp.num_tiles : max_units[dev];
+    cfg.gridDim = dim3(units * C::CTAS);
+    cudaError_t e;
     {
         LaunchScope ls(pr.name, s);
-        tc_gemm_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(kp);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, kp);
     }
+    if (e != cudaSuccess) return TPMLP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }
 
@@ -499,8 +586,10 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
 tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
     if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
     if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
-    if (pr.N <= 128) return launch<128>(pr, s);
-    return launch<256>(pr, s);
+    if (pr.N <= 128) return launch<128, false>(pr, s);
+    // a CTA pair covers 256 rows; below that the single-CTA tile wastes less
+    if (pr.M > 128) return launch<256, true>(pr, s);
+    return launch<256, false>(pr, s);
 }
 
 }  // namespace tpmlp

@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(256) colsum_kernel(const ColsumParams p) {
 
 constexpr int CE_THREADS = 256;
 constexpr int CE_WARPS = CE_THREADS / 32;
+constexpr int CE_MAX_UNITS = 16;     // max over T <= 16 of T * ceil(CE_WARPS / T)
+constexpr int CE_UNROLL = 8;         // independent 16-byte loads in flight per lane
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct CEParams {
@@ -184,6 +186,7 @@ struct CEParams {
     int32_t* owner;
     int64_t N, V, Vs;
     int T;
+    int parts;       // each shard is cut into `parts` contiguous pieces, one per warp
     int vec;
     int* err;
 };
@@ -205,6 +208,19 @@ __device__ __forceinline__ void lse_push(LseState& st, float x, int64_t idx) {
     }
 }
 
+// Four consecutive elements idx..idx+3; the first of equal maxima wins.
+__device__ __forceinline__ void lse_push4(LseState& st, float4 x, int64_t idx) {
+    const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+    if (mx > st.m) {
+        st.s *= exp2f((st.m - mx) * LOG2E);
+        st.m = mx;
+        st.a = idx + (x.x == mx ? 0 : (x.y == mx ? 1 : (x.z == mx ? 2 : 3)));
+    }
+    const float mL = st.m * LOG2E;
+    st.s += (exp2f(fmaf(x.x, LOG2E, -mL)) + exp2f(fmaf(x.y, LOG2E, -mL))) +
+            (exp2f(fmaf(x.z, LOG2E, -mL)) + exp2f(fmaf(x.w, LOG2E, -mL)));
+}
+
 // Merge two states: the larger max wins; on equal maxima the lower index.
 __device__ __forceinline__ void lse_merge(LseState& st, float m2, float s2, int64_t a2) {
     if (m2 == -INFINITY) return;
@@ -218,47 +234,40 @@ __device__ __forceinline__ void lse_merge(LseState& st, float m2, float s2, int6
     st.m = M;
 }
 
+// One CTA per token row. Unit u = (shard k = u / parts, piece u % parts) is a
+// contiguous range of shard k; warp w streams units w, w + CE_WARPS, ... with
+// coalesced 16-byte loads and reduces each unit with shuffles; one shared-
+// memory pass then combines the pieces of each shard and the shards.
 __global__ void __launch_bounds__(CE_THREADS) vocab_ce_kernel(const CEParams p) {
-    __shared__ float sm_m[kMaxG][CE_WARPS];
-    __shared__ float sm_s[kMaxG][CE_WARPS];
-    __shared__ long long sm_a[kMaxG][CE_WARPS];
+    __shared__ float sm_m[CE_MAX_UNITS];
+    __shared__ float sm_s[CE_MAX_UNITS];
+    __shared__ long long sm_a[CE_MAX_UNITS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t row = blockIdx.x;
     const float* z = p.logits + row * p.V;
+    const int units = p.T * p.parts;
 
-    for (int k = 0; k < p.T; ++k) {
+    for (int u = warp; u < units; u += CE_WARPS) {
+        const int k = u / p.parts, piece = u - k * p.parts;
         LseState st{-INFINITY, 0.f, 0x7fffffffffffffffLL};
         const int64_t base = (int64_t)k * p.Vs;
         if (p.vec) {
-            const float4* zv = reinterpret_cast<const float4*>(z + base);
             const int64_t n4 = p.Vs / 4;
-            int64_t i = threadIdx.x;
-            // four independent 16-byte loads in flight per thread
-            for (; i + 3 * CE_THREADS < n4; i += 4 * CE_THREADS) {
-                float4 x[4];
+            const int64_t lo = n4 * piece / p.parts, hi = n4 * (piece + 1) / p.parts;
+            const float4* zv = reinterpret_cast<const float4*>(z + base);
+            int64_t i = lo + lane;
+            for (; i + 32 * (CE_UNROLL - 1) < hi; i += 32 * CE_UNROLL) {
+                float4 x[CE_UNROLL];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) x[u] = __ldcs(zv + i + u * CE_THREADS);
+                for (int j = 0; j < CE_UNROLL; ++j) x[j] = __ldcs(zv + i + 32 * j);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t idx = base + 4 * (i + u * CE_THREADS);
-                    lse_push(st, x[u].x, idx);
-                    lse_push(st, x[u].y, idx + 1);
-                    lse_push(st, x[u].z, idx + 2);
-                    lse_push(st, x[u].w, idx + 3);
-                }
+                for (int j = 0; j < CE_UNROLL; ++j) lse_push4(st, x[j], base + 4 * (i + 32 * j));
             }
-            for (; i < n4; i += CE_THREADS) {
-                const float4 x = __ldcs(zv + i);
-                const int64_t idx = base + 4 * i;
-                lse_push(st, x.x, idx);
-                lse_push(st, x.y, idx + 1);
-                lse_push(st, x.z, idx + 2);
-                lse_push(st, x.w, idx + 3);
-            }
+            for (; i < hi; i += 32) lse_push4(st, __ldcs(zv + i), base + 4 * i);
         } else {
-            for (int64_t i = threadIdx.x; i < p.Vs; i += CE_THREADS) lse_push(st, z[base + i], base + i);
+            const int64_t lo = p.Vs * piece / p.parts, hi = p.Vs * (piece + 1) / p.parts;
+            for (int64_t i = lo + lane; i < hi; i += 32) lse_push(st, z[base + i], base + i);
         }
-        // warp combine
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, st.m, off);
@@ -267,17 +276,20 @@ __global__ void __launch_bounds__(CE_THREADS) vocab_ce_kernel(const CEParams p) 
             lse_merge(st, m2, s2, a2);
         }
         if (lane == 0) {
-            sm_m[k][warp] = st.m;
-            sm_s[k][warp] = st.s;
-            sm_a[k][warp] = st.a;
+            sm_m[u] = st.m;
+            sm_s[u] = st.s;
+            sm_a[u] = st.a;
         }
     }
     __syncthreads();
     if (warp != 0) return;
-    // lane k < T combines shard k over the warps of the CTA
+    // lane k < T: merge the pieces of shard k -> (m_k, s_k, argmax_k)
     LseState sh{-INFINITY, 0.f, 0x7fffffffffffffffLL};
     if (lane < p.T) {
-        for (int w = 0; w < CE_WARPS; ++w) lse_merge(sh, sm_m[lane][w], sm_s[lane][w], sm_a[lane][w]);
+        for (int q = 0; q < p.parts; ++q) {
+            const int u = lane * p.parts + q;
+            lse_merge(sh, sm_m[u], sm_s[u], sm_a[u]);
+        }
     }
     // combine the shards: m = max_k m_k, S = sum_k s_k exp(m_k - m)
     float m = sh.m;
@@ -408,6 +420,7 @@ tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
         kp.V = V;
         kp.Vs = V / T;
         kp.T = T;
+        kp.parts = (CE_WARPS + T - 1) / T;
         kp.vec = (kp.Vs % 4 == 0) && aligned16(logits);
         kp.err = device_error_word();
         if (kp.err == nullptr) return TPMLP_ERR_CUDA;
