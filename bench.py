@@ -146,32 +146,48 @@ class ClockSampler:
 class Block:
     """Device-resident inputs, outputs and workspace of one fwd+bwd step."""
 
-    def __init__(self, cfg, mode, dev):
+    def __init__(self, cfg, mode, dev, with_dy=True):
         import tensor_transformer_mlp_columnparallel_gb300 as tp
         self.tp = tp
         self.cfg, self.mode, self.dev = cfg, mode, dev
-        inp = gen_mlp_inputs(cfg)
+        inp = gen_mlp_inputs(cfg, with_dy=with_dy)
         self.host = inp
         self.X = inp.X.to(dev)
-        self.dY = inp.dY.to(dev)
+        self.dY = inp.dY.to(dev) if with_dy else None
         self.W1 = [w.to(dev) for w in inp.W1_shards()]
         self.W2 = [w.contiguous().to(dev) for w in inp.W2_shards()]
+        self.b1 = None if inp.b1 is None else [b.contiguous().to(dev) for b in inp.b1_shards()]
+        self.b2 = None if inp.b2 is None else inp.b2.to(dev)
         N, D, Fs, T = cfg.N, cfg.D, cfg.Fs, cfg.T
         dt = self.X.dtype
         e = lambda *s: torch.empty(s, dtype=dt, device=dev)
         self.Y = e(N, D)
         self.H = [e(N, Fs) for _ in range(T)]
         self.Z = [e(N, Fs) for _ in range(T)]
-        self.dX = e(N, D)
-        self.dW1 = [e(D, Fs) for _ in range(T)]
-        self.dW2 = [e(Fs, D) for _ in range(T)]
+        if with_dy:
+            self.dX = e(N, D)
+            self.dW1 = [e(D, Fs) for _ in range(T)]
+            self.dW2 = [e(Fs, D) for _ in range(T)]
         wf = tp.tpmlp_workspace_bytes(0, dt, N, D, cfg.F, T, mode)
-        wb = tp.tpmlp_workspace_bytes(1, dt, N, D, cfg.F, T, mode)
+        wb = tp.tpmlp_workspace_bytes(1, dt, N, D, cfg.F, T, mode) if with_dy else 0
         self.ws = torch.empty(max(wf, wb, 256), dtype=torch.uint8, device=dev)
+
+    def set_mode(self, mode):
+        tp = self.tp
+        cfg = self.cfg
+        self.mode = mode
+        need = max(tp.tpmlp_workspace_bytes(0, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode),
+                   tp.tpmlp_workspace_bytes(1, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode), 256)
+        if self.ws.numel() < need:
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.dev)
+
+    def forward(self):
+        self.tp.tpmlp_forward(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.H, self.Z,
+                              self.cfg.act, self.mode, self.ws)
 
     def step(self):
         tp = self.tp
-        tp.tpmlp_forward(self.X, self.W1, None, self.W2, None, self.Y, self.H, self.Z,
+        tp.tpmlp_forward(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.H, self.Z,
                          self.cfg.act, self.mode, self.ws)
         tp.tpmlp_backward(self.X, self.W1, self.W2, self.H, self.Z, self.dY, self.dX, self.dW1,
                           self.dW2, None, None, self.cfg.act, self.mode, self.ws)
@@ -225,15 +241,29 @@ def kernel_table(t, total_ms):
     return out
 
 
+def kernel_source_hash():
+    """sha256 over the library's CUDA sources (file name + bytes, sorted)."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "tensor_transformer_mlp_columnparallel_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
-    it is for the current build of that kernel (else None)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when that summary was taken on other
+    kernel sources than the ones built now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        return d.get(kernel, {}).get("dram_bytes_per_launch")
+        if d.get("source_hash") != kernel_source_hash():
+            return None
+        return d["kernels"].get(kernel, {}).get("dram_bytes_per_launch")
     except Exception:
         return None
 
@@ -285,6 +315,36 @@ def secondary(dev, stream, steps, pk):
                      "frac": gbs / pk["hbm_gbs"], "traffic": load_traffic("vocab_ce_fwd")}}
     del logits
     torch.cuda.empty_cache()
+    # forward-only workloads: N=4096 D=4096 F=16384 T=4 (tensor-bound) and
+    # N=16 D=12288 F=49152 T=8 (weight streaming, HBM-bound)
+    for name in ("mlp_bf16_gelu_n4096_d4096_f16384_t4", "mlp_bf16_gelu_n16_d12288_f49152_t8"):
+        fc = MLP_CONFIGS[name]
+        fb = Block(fc, "splitk", dev, with_dy=False)
+        for mode in ("splitk", "partials"):
+            fb.set_mode(mode)
+            tp.tpmlp_timing_reset()
+            tp.tpmlp_timing_enable(True)
+            ms_f = timed(fb.forward, steps, 3, 1, dev, stream)
+            tp.tpmlp_timing_enable(False)
+            t = tp.tpmlp_timing_read()
+            flops = fc.fwd_flops()
+            wbytes = 2.0 * fc.D * fc.F * 2 + fc.F * 2 + fc.D * 2      # W1, W2, b1, b2 (bf16)
+            abytes = wbytes + 2.0 * fc.N * fc.D * 2 + 2.0 * fc.N * fc.F * 2   # + X, Y, H, Z
+            rec = {"mode": mode, "ms_per_forward": ms_f / steps,
+                   "TFLOP/s": flops * steps / (ms_f * 1e-3) / 1e12,
+                   "GB/s": abytes * steps / (ms_f * 1e-3) / 1e9,
+                   "kernels": kernel_table(t, ms_f)}
+            if fc.N <= 64:
+                rec["roofline"] = {"bound": "hbm", "achieved": rec["GB/s"], "peak": pk["hbm_gbs"],
+                                   "unit": "GB/s", "frac": rec["GB/s"] / pk["hbm_gbs"],
+                                   "algorithmic_bytes_per_forward": abytes}
+            else:
+                rec["roofline"] = {"bound": "tensor", "achieved": rec["TFLOP/s"],
+                                   "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                                   "frac": rec["TFLOP/s"] / pk["bf16_tflops_sustained"]}
+            out[f"{name}_{mode}"] = rec
+        del fb
+        torch.cuda.empty_cache()
     # the PARTIALS variant of the same fwd+bwd step: T fp32 partials + block reduce
     cfg = MLP_CONFIGS[WORKLOAD]
     blk = Block(cfg, "partials", dev)

@@ -56,11 +56,15 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
-    static constexpr int STAGES = STAGE_BYTES <= 32768 ? 6 : 4;
+    // as many stages as fit in 227 KB next to the barriers and the 1 KB alignment slack
+    static constexpr int SMEM_LIMIT = 232448;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
     static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
     static_assert(B_ROWS % BOX_MN == 0, "MN-major B boxes");
 };
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 for (int kb = 0; kb < kb_total; ++kb) {
                     const int gk = p.fold ? kb / kb_per_group : g;
                     const int k0 = (p.fold ? kb - gk * kb_per_group : kb) * BK;
-                    if (!wait_bounded(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                    if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
                     }
@@ -357,30 +361,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const uint32_t b_lbo = p.b_mn ? MN_BOX_BYTES : 16;
             const uint32_t a_kstep = p.a_mn ? UMMA_K * 128 : UMMA_K * 2;
             const uint32_t b_kstep = p.b_mn ? UMMA_K * 128 : UMMA_K * 2;
+            const uint64_t a_desc0 = smem_desc(sA0, a_lbo, 1024);
+            const uint64_t b_desc0 = smem_desc(sB0, b_lbo, 1024);
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
             for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
-                if (!wait_bounded(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                if (!wait_fast(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < kb_total; ++kb) {
-                    if (!wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, true)) {
+                    if (!wait_fast(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = sA0 + s * C::A_BYTES;
-                    const uint32_t b_base = sB0 + s * C::B_BYTES;
+                    // the start-address field is the low 14 bits (16-byte units): one
+                    // add per K step, the rest of the descriptor is fixed
+                    const uint64_t ad0 = a_desc0 + (uint64_t)((s * C::A_BYTES) >> 4);
+                    const uint64_t bd0 = b_desc0 + (uint64_t)((s * C::B_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
-                        const uint64_t ad = smem_desc(a_base + k * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc(b_base + k * b_kstep, b_lbo, 1024);
+                        const uint64_t ad = ad0 + (uint64_t)((k * a_kstep) >> 4);
+                        const uint64_t bd = bd0 + (uint64_t)((k * b_kstep) >> 4);
                         if constexpr (PAIR)
                             tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
             // one lane waits; the warp stays converged for the .sync.aligned TMEM loads
             int ok = 1;
-            if (lane == 0) ok = wait_bounded(bar(TFULL + acc), aph, abort_flag, p.err, p.timeout_ns, true);
+            if (lane == 0) ok = wait_fast(bar(TFULL + acc), aph, abort_flag, p.err, p.timeout_ns, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -586,9 +594,38 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
 tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
     if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
     if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
-    if (pr.N <= 128) return launch<128, false>(pr, s);
-    // a CTA pair covers 256 rows; below that the single-CTA tile wastes less
-    if (pr.M > 128) return launch<256, true>(pr, s);
+    // Tile choice by estimated time = waves x per-tile cost. A wave is one
+    // tile per CTA (single) or per CTA pair; the per-tile cost is its MMA work
+    // over the relative rate measured for the tile shape, or, for a few rows
+    // (M <= 64: weight streaming, HBM-bound), the operand bytes it streams,
+    // which grow with BN.
+    struct Cand {
+        int bn;
+        bool pair;
+        double rate;
+    };
+    const Cand cands[3] = {{256, true, 1.08}, {256, false, 1.0}, {128, false, 0.85}};
+    const int sms = device_sm_count();
+    const int groups = pr.fold ? 1 : pr.G;
+    double best = 1e300;
+    int pick = 1;
+    for (int i = 0; i < 3; ++i) {
+        const Cand& c = cands[i];
+        if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
+        const int64_t tile_m = c.pair ? 256 : 128;
+        const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
+                              ((pr.N + c.bn - 1) / c.bn);
+        const int64_t units = c.pair ? sms / 2 : sms;
+        const int64_t waves = (tiles + units - 1) / units;
+        const double cost = pr.M <= 64 ? (double)waves * c.bn
+                                        : (double)waves * 128.0 * c.bn / c.rate;
+        if (cost < best) {
+            best = cost;
+            pick = i;
+        }
+    }
+    if (cands[pick].bn == 128) return launch<128, false>(pr, s);
+    if (cands[pick].pair) return launch<256, true>(pr, s);
     return launch<256, false>(pr, s);
 }
 

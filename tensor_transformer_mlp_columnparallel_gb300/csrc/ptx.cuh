@@ -76,6 +76,14 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
     }
 }
 
+// Inline fast path: one try_wait, and only when the phase is not complete yet
+// the out-of-line bounded wait.
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, uint64_t timeout_ns, bool watch_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort_flag, err, timeout_ns, watch_abort);
+}
+
 // ---- clusters -------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
