@@ -313,7 +313,75 @@ def secondary(dev, stream, steps, pk):
         "kernel": "vocab_ce_fwd", "ms_per_launch": ms, "GB/s": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"], "traffic": load_traffic("vocab_ce_fwd")}}
-    del logits
+    # backward of the same cross-entropy (mean reduction): read z, write dz
+    dlog = torch.empty_like(logits)
+    fnb = lambda: tp.tpmlp_vocab_ce_backward(logits, targets, ce.T, loss, 1.0 / ce.N, dlog)
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    timed(fnb, steps, 3, 1, dev, stream)
+    tp.tpmlp_timing_enable(False)
+    t = tp.tpmlp_timing_read()
+    k = t["vocab_ce_bwd"]
+    ms = k["total_ms"] / k["launches"]
+    bwd_bytes = 8.0 * ce.N * ce.V + 12.0 * ce.N
+    gbs = bwd_bytes / (ms * 1e-3) / 1e9
+    out["vocab_ce_backward_n8192_v128000_t8"] = {
+        "kernel": "vocab_ce_bwd", "ms_per_launch": ms, "GB/s": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": load_traffic("vocab_ce_bwd"),
+                     "algorithmic_bytes_per_launch": bwd_bytes}}
+    del logits, dlog
+    torch.cuda.empty_cache()
+    # block end as a reduce-scatter (T = 8 fp32 partials of [8192, 8192] -> 8 bf16
+    # row blocks of [1024, 8192]); the partials exceed L2
+    Tn, Nn, Dn = 8, 8192, 8192
+    parts = [torch.randn(Nn, Dn, device=dev) for _ in range(Tn)]
+    rows_out = [torch.empty(Nn // Tn, Dn, dtype=torch.bfloat16, device=dev) for _ in range(Tn)]
+    b2 = torch.zeros(Dn, dtype=torch.bfloat16, device=dev)
+    fn = lambda: tp.tpmlp_block_reduce_scatter(parts, b2, rows_out)
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    timed(fn, steps, 3, 1, dev, stream)
+    tp.tpmlp_timing_enable(False)
+    k = tp.tpmlp_timing_read()["block_reduce_scatter_bias"]
+    ms = k["total_ms"] / k["launches"]
+    rs_bytes = Tn * Nn * Dn * 4 + Nn * Dn * 2 + Dn * 2
+    gbs = rs_bytes / (ms * 1e-3) / 1e9
+    out["block_reduce_scatter_t8_n8192_d8192"] = {
+        "kernel": "block_reduce_scatter_bias", "ms_per_launch": ms, "GB/s": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": rs_bytes,
+                     "traffic": load_traffic("block_reduce_scatter_bias")}}
+    del parts, rows_out
+    torch.cuda.empty_cache()
+    # vocab-parallel embedding: table 32000 x 8192 bf16 over T = 4 (the textbook
+    # page's row-parallel embedding), 8192 tokens; L2 flushed before every launch
+    Ve, He, Te, Ne = 32000, 8192, 4, 8192
+    ge = torch.Generator(device=dev)
+    ge.manual_seed(0)
+    shards = [(torch.randn(Ve // Te, He, generator=ge, device=dev) * 0.02).to(torch.bfloat16)
+              for _ in range(Te)]
+    ids = torch.randint(0, Ve, (Ne,), generator=ge, device=dev)
+    emb = torch.empty(Ne, He, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    tp.tpmlp_timing_reset()
+    for i in range(3 + steps):
+        flush.fill_(i & 0xff)
+        if i == 3:
+            tp.tpmlp_timing_enable(True)
+        tp.tpmlp_vocab_embedding(ids, shards, emb)
+    torch.cuda.synchronize()
+    tp.tpmlp_timing_enable(False)
+    k = tp.tpmlp_timing_read()["vocab_embedding"]
+    ms = k["total_ms"] / k["launches"]
+    e_bytes = 2.0 * Ne * He * 2 + Ne * 8
+    gbs = e_bytes / (ms * 1e-3) / 1e9
+    out["vocab_embedding_v32000_h8192_t4_n8192"] = {
+        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs, "l2": "flushed before each launch",
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": e_bytes,
+                     "traffic": load_traffic("vocab_embedding")}}
+    del shards, emb, flush
     torch.cuda.empty_cache()
     # forward-only workloads: N=4096 D=4096 F=16384 T=4 (tensor-bound) and
     # N=16 D=12288 F=49152 T=8 (weight streaming, HBM-bound)

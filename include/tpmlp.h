@@ -120,6 +120,45 @@ tpmlp_status tpmlp_block_reduce(tpmlp_dtype dt, int64_t N, int64_t D, int T,
                                 const float* const* partials, const void* b2, void* Y,
                                 void* stream);
 
+/* Reduce-scatter form of the block end (§04: the all-reduce may become a
+ * reduce-scatter so that the output stays sharded by tokens): the same sum
+ * Y = sum_r P^(r) + b2 as tpmlp_block_reduce, with rows [r N/T, (r+1) N/T)
+ * written to Y_rows[r].
+ *   partials  T x [N, D] fp32
+ *   b2        [D] (element type dt) or NULL
+ *   Y_rows    host array of T device pointers, each [N/T, D] of dt
+ * Errors: TPMLP_ERR_SHAPE if N % T != 0. */
+tpmlp_status tpmlp_block_reduce_scatter(tpmlp_dtype dt, int64_t N, int64_t D, int T,
+                                        const float* const* partials, const void* b2,
+                                        void* const* Y_rows, void* stream);
+
+/* tpmlp_forward whose block end is the reduce-scatter: the same arguments,
+ * with Y replaced by Y_rows (T device pointers, each [N/T, D]); rank r's row
+ * block of Y lands in Y_rows[r]. In SPLITK mode the split-K row GEMM writes
+ * each output row straight into its block; in PARTIALS mode the reduce kernel
+ * scatters. Errors: those of tpmlp_forward, and TPMLP_ERR_SHAPE if N % T != 0. */
+tpmlp_status tpmlp_forward_reduce_scatter(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                          tpmlp_act act, const void* X, const void* const* W1,
+                                          const void* const* b1, const void* const* W2,
+                                          const void* b2, void* const* Y_rows, void* const* H,
+                                          void* const* Z, tpmlp_reduce_mode mode, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* Vocab-parallel embedding lookup (textbook page §4.2.3 row-parallel
+ * embedding; course notes §3.4 "TP for Embedding"): the table [V, Hd] is split
+ * by rows into T shards of V/T rows; shard k returns its row for ids in
+ * [k V/T, (k+1) V/T) and zeros otherwise, and the sum over shards (the
+ * all-reduce) is the embedding. On one GPU every token's row is copied from
+ * its owning shard, which is that sum exactly.
+ *   ids    [N] int64
+ *   table  host array of T device pointers, each [V/T, Hd] of dt
+ *   out    [N, Hd] of dt
+ * Errors: TPMLP_ERR_SHAPE if V % T != 0. An id outside [0, V) gets a zero row
+ * (no shard owns it) and sets TPMLP_ERR_ARG in the device error word. */
+tpmlp_status tpmlp_vocab_embedding(tpmlp_dtype dt, int64_t N, int64_t V, int64_t Hd, int T,
+                                   const int64_t* ids, const void* const* table, void* out,
+                                   void* stream);
+
 /* Vocab-parallel cross-entropy forward (see the header comment).
  *   logits          [N, V] fp32; shard k owns columns [k*V/T, (k+1)*V/T)
  *   targets         [N] int64 in [0, V)
@@ -132,6 +171,22 @@ tpmlp_status tpmlp_block_reduce(tpmlp_dtype dt, int64_t N, int64_t D, int T,
 tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
                             const int64_t* targets, float* loss_per_token, float* loss_mean,
                             int32_t* argmax, int32_t* target_owner, void* stream);
+
+/* Vocab-parallel cross-entropy backward (course notes §3.6.4, first step):
+ *   dlogits[n, v] = grad_scale * (exp(z[n, v] - lse_n) - 1(v = t_n))
+ * Every vocab shard's slice needs only the forward's per-token result, no
+ * exchange of logits: lse_n = m_n + ln S_n is recovered as
+ * loss_per_token[n] + z[n, t_n].
+ *   logits          [N, V] fp32 (the forward's input)
+ *   targets         [N] int64 in [0, V)
+ *   loss_per_token  [N] fp32, as written by tpmlp_vocab_ce for these logits
+ *   grad_scale      upstream gradient of each token's loss (1/N for the mean)
+ *   dlogits         [N, V] fp32 out; may be the logits buffer itself (in place)
+ * Errors: TPMLP_ERR_SHAPE if V % T != 0; a target outside [0, V) writes NaN
+ * for that row and sets TPMLP_ERR_ARG in the device error word. */
+tpmlp_status tpmlp_vocab_ce_backward(int64_t N, int64_t V, int T, const float* logits,
+                                     const int64_t* targets, const float* loss_per_token,
+                                     float grad_scale, float* dlogits, void* stream);
 
 /* Size in bytes of the library's own scratch array (see tpmlp_forward_noalloc). */
 #define TPMLP_NOALLOC_SCRATCH_BYTES (8u << 20)

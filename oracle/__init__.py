@@ -18,6 +18,10 @@ What it computes (plain definitions, no blocking, fusion or reordering):
   over tokens, argmax per token and the shard that owns each target
   (page "unpurerationalist ... 3.4 TP for Embedding", LM head bullets;
   Megatron TP chapter §7.8).
+- ``ce.vocab_ce_backward``: grad_scale * (softmax(z) - onehot(t)) (course
+  notes §3.6.4).
+- ``embedding.vocab_embedding``: out[n] = E[ids[n]] (textbook §4.2.3, course
+  notes §3.4 "TP for Embedding").
 - ``sharded``: the per-shard algorithm (column shard -> local activation ->
   row shard partial -> sum), used ONLY to pin the claim that sharding leaves
   the result unchanged. The unsharded functions above are the oracle.
@@ -32,4 +36,4 @@ torch.logsumexp for the cross-entropy. Every function here has at least one
 pin; none is "parity unpinned".
 """
 
-from . import mlp, ce, sharded  # noqa: F401
+from . import mlp, ce, sharded, embedding  # noqa: F401

@@ -71,6 +71,36 @@ def block_reduce(partials, b2):
     return out
 
 
+def block_reduce_scatter(partials, b2, T):
+    """Reduce-scatter form of the block end (page "一层 MLP 太宽而放不下时怎样切？",
+    §04): the sum of the full-shape partials is split by tokens, rank r keeping
+    rows [r N/T, (r+1) N/T). Returns the T row blocks."""
+    Y = block_reduce(partials, b2)
+    N = Y.shape[0]
+    if N % T != 0:
+        raise ValueError("N must be divisible by T")
+    Ns = N // T
+    return [Y[r * Ns:(r + 1) * Ns] for r in range(T)]
+
+
+def vocab_embedding_sharded(ids, table, T):
+    """Row-split embedding (textbook page §4.2.3; course notes §3.4): shard k
+    holds rows [k V/T, (k+1) V/T); for every token it returns its local row, or
+    zeros when the id lies outside its range; the T results are summed."""
+    E = as_f64(table)
+    ids = np.asarray(ids, dtype=np.int64)
+    V, Hd = E.shape
+    Vs = V // T
+    out = np.zeros((ids.shape[0], Hd))
+    for k in range(T):
+        local = ids - k * Vs
+        mine = (local >= 0) & (local < Vs)
+        part = np.zeros_like(out)
+        part[mine] = E[k * Vs:(k + 1) * Vs][local[mine]]
+        out = out + part
+    return out
+
+
 def backward_dx(X, W1, b1, W2, dY, kind, T):
     """Per-shard dX contributions dZ^(r) W1^(r)^T and their sum."""
     X, dY = as_f64(X), as_f64(dY)
@@ -121,3 +151,24 @@ def vocab_ce_sharded(logits, targets, T):
     owner = t // Vs
     zt = np.array([z[n, k * Vs + (t[n] - k * Vs)] for n, k in enumerate(owner)])
     return {"m_k": m_k, "s_k": s_k, "loss": m + np.log(S) - zt, "owner": owner}
+
+
+def vocab_ce_backward_sharded(logits, targets, T, grad_scale):
+    """Shard k computes its own slice from the global (m, S) of the forward:
+    dz_k = g * (exp(z_k - m) / S - 1(v = t)), then the slices are concatenated."""
+    z = as_f64(logits)
+    t = np.asarray(targets, dtype=np.int64)
+    N, V = z.shape
+    Vs = V // T
+    fwd = vocab_ce_sharded(z, t, T)
+    m = fwd["m_k"].max(axis=1)
+    S = (fwd["s_k"] * np.exp(fwd["m_k"] - m[:, None])).sum(axis=1)
+    parts = []
+    for k in range(T):
+        zk = z[:, k * Vs:(k + 1) * Vs]
+        dk = np.exp(zk - m[:, None]) / S[:, None]
+        for n in range(N):
+            if k * Vs <= t[n] < (k + 1) * Vs:
+                dk[n, t[n] - k * Vs] -= 1.0
+        parts.append(grad_scale * dk)
+    return np.concatenate(parts, axis=1)

@@ -16,9 +16,11 @@ from ._binding import (  # noqa: F401
     TpmlpError,
     tpmlp_backward,
     tpmlp_block_reduce,
+    tpmlp_block_reduce_scatter,
     tpmlp_check_device_error,
     tpmlp_forward,
     tpmlp_forward_noalloc,
+    tpmlp_forward_reduce_scatter,
     tpmlp_launch_count,
     tpmlp_selftest_wait_timeout,
     tpmlp_set_wait_timeout_ns,
@@ -26,6 +28,8 @@ from ._binding import (  # noqa: F401
     tpmlp_timing_read,
     tpmlp_timing_reset,
     tpmlp_vocab_ce,
+    tpmlp_vocab_ce_backward,
+    tpmlp_vocab_embedding,
     tpmlp_workspace_bytes,
 )
 
@@ -96,3 +100,35 @@ def block_reduce(partials: List[torch.Tensor], b2: Optional[torch.Tensor], out_d
     Y = torch.empty((N, D), dtype=out_dtype, device=partials[0].device)
     tpmlp_block_reduce(partials, b2, Y)
     return Y
+
+
+def vocab_ce_backward(logits: torch.Tensor, targets: torch.Tensor, T: int,
+                      loss_per_token: torch.Tensor, grad_scale: float, in_place: bool = False):
+    """Gradient of grad_scale * sum_n loss_n with respect to the logits."""
+    d = logits if in_place else torch.empty_like(logits)
+    tpmlp_vocab_ce_backward(logits, targets, T, loss_per_token, grad_scale, d)
+    return d
+
+
+def mlp_forward_reduce_scatter(X, W1, W2, b1=None, b2=None, act: str = "gelu_tanh",
+                               mode: str = "splitk", save_z: bool = True):
+    """Forward whose block end is a reduce-scatter: returns (Y_rows list of T
+    [N/T, D], H, Z)."""
+    T = len(W1)
+    N, D = X.shape
+    Fs = W1[0].shape[1]
+    dev, dt = X.device, X.dtype
+    Y_rows = [torch.empty((N // T, D), dtype=dt, device=dev) for _ in range(T)]
+    H = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)]
+    Z = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_z else None
+    ws = _workspace(tpmlp_workspace_bytes(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
+    tpmlp_forward_reduce_scatter(X, list(W1), list(b1) if b1 is not None else None, list(W2), b2,
+                                 Y_rows, H, Z, act, mode, ws)
+    return Y_rows, H, Z
+
+
+def vocab_embedding(ids: torch.Tensor, table: Sequence[torch.Tensor]):
+    """Embedding rows of `ids` from a table split by rows into len(table) shards."""
+    out = torch.empty((ids.shape[0], table[0].shape[1]), dtype=table[0].dtype, device=ids.device)
+    tpmlp_vocab_embedding(ids, list(table), out)
+    return out

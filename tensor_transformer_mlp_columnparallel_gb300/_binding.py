@@ -52,7 +52,12 @@ _SIGNATURES = {
     "tpmlp_backward": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _PP, _vp,
                               _vp, _PP, _PP, _PP, _vp, _int, _vp, ctypes.c_size_t, _vp]),
     "tpmlp_block_reduce": (_int, [_int, _i64, _i64, _int, _PP, _vp, _vp, _vp]),
+    "tpmlp_block_reduce_scatter": (_int, [_int, _i64, _i64, _int, _PP, _vp, _PP, _vp]),
+    "tpmlp_forward_reduce_scatter": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP,
+                                            _vp, _PP, _PP, _PP, _int, _vp, ctypes.c_size_t, _vp]),
+    "tpmlp_vocab_embedding": (_int, [_int, _i64, _i64, _i64, _int, _vp, _PP, _vp, _vp]),
     "tpmlp_vocab_ce": (_int, [_i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "tpmlp_vocab_ce_backward": (_int, [_i64, _i64, _int, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "tpmlp_workspace_bytes": (ctypes.c_size_t, [_int, _int, _i64, _i64, _i64, _int, _int]),
     "tpmlp_status_str": (ctypes.c_char_p, [_int]),
     "tpmlp_check_device_error": (_int, [_vp]),
@@ -196,6 +201,39 @@ def tpmlp_block_reduce(partials: Sequence[torch.Tensor], b2, Y):
                                     _stream(Y)))
 
 
+def tpmlp_block_reduce_scatter(partials: Sequence[torch.Tensor], b2, Y_rows: Sequence[torch.Tensor]):
+    """Rows [r N/T, (r+1) N/T) of sum_r partials[r] + b2 into Y_rows[r]."""
+    T = len(partials)
+    N, D = partials[0].shape
+    _require([*partials, b2, *Y_rows], partials[0].device, None)
+    _check(lib().tpmlp_block_reduce_scatter(_dtype_code(Y_rows[0]), N, D, T, _ptrs(partials),
+                                            _ptr(b2), _ptrs(Y_rows), _stream(partials[0])))
+
+
+def tpmlp_forward_reduce_scatter(X, W1, b1, W2, b2, Y_rows, H, Z, act: str, mode: str,
+                                 workspace=None):
+    """tpmlp_forward with the reduce-scatter block end: rank r's rows in Y_rows[r]."""
+    T = len(W1)
+    N, D = X.shape
+    Fs = W1[0].shape[1]
+    _require([X, b2, workspace, *Y_rows, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, None)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tpmlp_forward_reduce_scatter(
+        _dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X), _ptrs(W1), _ptrs(b1), _ptrs(W2),
+        _ptr(b2), _ptrs(Y_rows), _ptrs(H), _ptrs(Z), MODE[mode], _ptr(workspace), ws_bytes,
+        _stream(X)))
+
+
+def tpmlp_vocab_embedding(ids, table: Sequence[torch.Tensor], out):
+    """out[n] = table row ids[n] (table split by rows into len(table) shards)."""
+    T = len(table)
+    Vs, Hd = table[0].shape
+    _require([ids], out.device, torch.int64)
+    _require([*table, out], out.device, out.dtype)
+    _check(lib().tpmlp_vocab_embedding(_dtype_code(out), ids.shape[0], Vs * T, Hd, T, _ptr(ids),
+                                       _ptrs(table), _ptr(out), _stream(out)))
+
+
 def tpmlp_vocab_ce(logits, targets, T: int, loss_per_token, loss_mean=None, argmax=None,
                    target_owner=None):
     """Vocab-parallel cross-entropy over T contiguous vocab shards."""
@@ -207,6 +245,16 @@ def tpmlp_vocab_ce(logits, targets, T: int, loss_per_token, loss_mean=None, argm
     _check(lib().tpmlp_vocab_ce(N, V, T, _ptr(logits), _ptr(targets), _ptr(loss_per_token),
                                 _ptr(loss_mean), _ptr(argmax), _ptr(target_owner),
                                 _stream(logits)))
+
+
+def tpmlp_vocab_ce_backward(logits, targets, T: int, loss_per_token, grad_scale: float, dlogits):
+    """dlogits = grad_scale * (softmax(logits) - onehot(targets)); dlogits may
+    be logits itself (in place)."""
+    N, V = logits.shape
+    _require([logits, loss_per_token, dlogits], logits.device, torch.float32)
+    _require([targets], logits.device, torch.int64)
+    _check(lib().tpmlp_vocab_ce_backward(N, V, T, _ptr(logits), _ptr(targets), _ptr(loss_per_token),
+                                         float(grad_scale), _ptr(dlogits), _stream(logits)))
 
 
 def tpmlp_check_device_error(device=None) -> int:

@@ -210,17 +210,25 @@ size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, 
     return (size_t)-1;
 }
 
-tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
-                           const void* X, const void* const* W1, const void* const* b1,
-                           const void* const* W2, const void* b2, void* Y, void* const* H,
-                           void* const* Z, tpmlp_reduce_mode mode, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+// The forward's steps; the block end writes Y, or, with Y_rows, row block r
+// of Y to Y_rows[r] (reduce-scatter).
+static tpmlp_status forward_impl(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                 tpmlp_act act, const void* X, const void* const* W1,
+                                 const void* const* b1, const void* const* W2, const void* b2,
+                                 void* Y, void* const* Y_rows, void* const* H, void* const* Z,
+                                 tpmlp_reduce_mode mode, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
     TPMLP_TRY(check_dims(dt, N, D, F, T, act));
     if (mode != TPMLP_REDUCE_PARTIALS && mode != TPMLP_REDUCE_SPLITK) return TPMLP_ERR_ARG;
     if (N == 0) return TPMLP_OK;   // every output is empty
     const bool bf = dt == TPMLP_BF16;
     TPMLP_TRY(check_ptr(X, bf));
-    TPMLP_TRY(check_ptr(Y, bf));
+    if (Y_rows != nullptr) {
+        if (N % T != 0) return TPMLP_ERR_SHAPE;
+        TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(Y_rows), T, bf));
+    } else {
+        TPMLP_TRY(check_ptr(Y, bf));
+    }
     TPMLP_TRY(check_shards(W1, T, bf));
     TPMLP_TRY(check_shards(W2, T, bf));
     TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(H), T, bf));
@@ -268,14 +276,22 @@ tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int 
             parts[r] = pr;
         }
         TPMLP_TRY(run_gemm(dt, row, s));
-        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s, "block_reduce_bias"));
+        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s,
+                                   Y_rows ? "block_reduce_scatter_bias" : "block_reduce_bias",
+                                   Y_rows));
     } else {
-        GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1, "row_gemm_splitk_bias");
+        GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1,
+                                  Y_rows ? "row_gemm_splitk_bias_scatter" : "row_gemm_splitk_bias");
         row.epi.kind = EPI_STORE;
         row.epi.out_f32 = f32;
         row.epi.ldc = D;
-        row.epi.C[0] = Y;
         row.epi.bias[0] = b2;
+        if (Y_rows != nullptr) {
+            row.epi.row_shard = N / T;
+            for (int r = 0; r < T; ++r) row.epi.C[r] = Y_rows[r];
+        } else {
+            row.epi.C[0] = Y;
+        }
         for (int r = 0; r < T; ++r) {
             row.A[r] = H[r];
             row.B[r] = W2[r];
@@ -283,6 +299,26 @@ tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int 
         TPMLP_TRY(run_gemm(dt, row, s));
     }
     return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
+                           const void* X, const void* const* W1, const void* const* b1,
+                           const void* const* W2, const void* b2, void* Y, void* const* H,
+                           void* const* Z, tpmlp_reduce_mode mode, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return forward_impl(dt, N, D, F, T, act, X, W1, b1, W2, b2, Y, nullptr, H, Z, mode, workspace,
+                        workspace_bytes, stream);
+}
+
+tpmlp_status tpmlp_forward_reduce_scatter(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                          tpmlp_act act, const void* X, const void* const* W1,
+                                          const void* const* b1, const void* const* W2,
+                                          const void* b2, void* const* Y_rows, void* const* H,
+                                          void* const* Z, tpmlp_reduce_mode mode, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    if (Y_rows == nullptr) return TPMLP_ERR_ARG;
+    return forward_impl(dt, N, D, F, T, act, X, W1, b1, W2, b2, nullptr, Y_rows, H, Z, mode,
+                        workspace, workspace_bytes, stream);
 }
 
 tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
@@ -426,6 +462,33 @@ tpmlp_status tpmlp_block_reduce(tpmlp_dtype dt, int64_t N, int64_t D, int T,
                             static_cast<cudaStream_t>(stream), "block_reduce_bias");
 }
 
+tpmlp_status tpmlp_block_reduce_scatter(tpmlp_dtype dt, int64_t N, int64_t D, int T,
+                                        const float* const* partials, const void* b2,
+                                        void* const* Y_rows, void* stream) {
+    if (dt != TPMLP_F32 && dt != TPMLP_BF16) return TPMLP_ERR_DTYPE;
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (D <= 0 || T < 1 || T > TPMLP_MAX_SHARDS || N % T != 0) return TPMLP_ERR_SHAPE;
+    if (partials == nullptr || Y_rows == nullptr) return TPMLP_ERR_ARG;
+    for (int r = 0; r < T; ++r)
+        if (partials[r] == nullptr || Y_rows[r] == nullptr) return TPMLP_ERR_ARG;
+    return run_block_reduce(dt == TPMLP_F32, N, D, T, partials, b2, nullptr,
+                            static_cast<cudaStream_t>(stream), "block_reduce_scatter_bias", Y_rows);
+}
+
+tpmlp_status tpmlp_vocab_embedding(tpmlp_dtype dt, int64_t N, int64_t V, int64_t Hd, int T,
+                                   const int64_t* ids, const void* const* table, void* out,
+                                   void* stream) {
+    if (dt != TPMLP_F32 && dt != TPMLP_BF16) return TPMLP_ERR_DTYPE;
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (V <= 0 || Hd <= 0 || T < 1 || T > TPMLP_MAX_SHARDS || V % T != 0) return TPMLP_ERR_SHAPE;
+    if (N > 0 && (ids == nullptr || out == nullptr || table == nullptr)) return TPMLP_ERR_ARG;
+    if (table != nullptr)
+        for (int k = 0; k < T; ++k)
+            if (table[k] == nullptr) return TPMLP_ERR_ARG;
+    return run_vocab_embedding(dt == TPMLP_F32, N, V, Hd, T, ids, table, out,
+                               static_cast<cudaStream_t>(stream));
+}
+
 tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
                             const int64_t* targets, float* loss_per_token, float* loss_mean,
                             int32_t* argmax, int32_t* target_owner, void* stream) {
@@ -436,6 +499,19 @@ tpmlp_status tpmlp_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
     if (V > 0x7fffffffLL || N > 0x7fffffffLL) return TPMLP_ERR_SHAPE;
     return run_vocab_ce(N, V, T, logits, targets, loss_per_token, loss_mean, argmax, target_owner,
                         static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_vocab_ce_backward(int64_t N, int64_t V, int T, const float* logits,
+                                     const int64_t* targets, const float* loss_per_token,
+                                     float grad_scale, float* dlogits, void* stream) {
+    if (N < 0) return TPMLP_ERR_ARG;
+    if (V <= 0 || T < 1 || T > TPMLP_MAX_SHARDS || V % T != 0) return TPMLP_ERR_SHAPE;
+    if (V > 0x7fffffffLL || N > 0x7fffffffLL) return TPMLP_ERR_SHAPE;
+    if (N > 0 && (logits == nullptr || targets == nullptr || loss_per_token == nullptr ||
+                  dlogits == nullptr))
+        return TPMLP_ERR_ARG;
+    return run_vocab_ce_backward(N, V, logits, targets, loss_per_token, grad_scale, dlogits,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 const char* tpmlp_status_str(tpmlp_status s) {

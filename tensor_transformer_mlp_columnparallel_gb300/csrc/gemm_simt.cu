@@ -27,7 +27,13 @@ __device__ __forceinline__ void epi_scalar(const EpiArgs& e, int g, int m, int n
     } else if (e.kind == EPI_DACT) {
         v *= act_grad(e.act, static_cast<const float*>(e.aux[g])[(int64_t)m * e.ldaux + n]);
     }
-    static_cast<float*>(e.C[g])[(int64_t)m * e.ldc + n] = v;
+    int cg = g;
+    int64_t crow = m;
+    if (e.row_shard > 0) {
+        cg = (int)(m / e.row_shard);
+        crow = m - (int64_t)cg * e.row_shard;
+    }
+    static_cast<float*>(e.C[cg])[crow * e.ldc + n] = v;
 }
 
 template <bool A_MN, bool B_MN>

@@ -223,8 +223,14 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
                 if (col0 + j < N) v[j] *= act_grad(e.act, bf2f(z[j]));
         }
     }
+    int cg = g;
+    int64_t crow = row;
+    if (e.row_shard > 0) {          // reduce-scatter output: row block i -> C[i]
+        cg = (int)(row / e.row_shard);
+        crow = row - (int64_t)cg * e.row_shard;
+    }
     if (e.out_f32) {
-        float* c = static_cast<float*>(e.C[g]) + (int64_t)row * e.ldc + col0;
+        float* c = static_cast<float*>(e.C[cg]) + crow * e.ldc + col0;
         if (full) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -236,7 +242,7 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
                 if (col0 + j < N) c[j] = v[j];
         }
     } else {
-        __nv_bfloat16* c = static_cast<__nv_bfloat16*>(e.C[g]) + (int64_t)row * e.ldc + col0;
+        __nv_bfloat16* c = static_cast<__nv_bfloat16*>(e.C[cg]) + crow * e.ldc + col0;
         if (full) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

@@ -32,7 +32,18 @@ struct ReduceParams {
     int64_t N, D;
     const void* bias;
     void* Y;
+    void* Yr[kMaxG];      // reduce-scatter: row block i of Y goes to Yr[i]
+    int64_t rows_per;     // rows per block (0: plain reduce into Y)
 };
+
+// Destination element offset (in elements of OutT) of flat output index e.
+template <typename OutT>
+__device__ __forceinline__ OutT* reduce_dst(const ReduceParams& p, int64_t e) {
+    if (p.rows_per == 0) return static_cast<OutT*>(p.Y) + e;
+    const int64_t row = e / p.D;
+    const int64_t blk = row / p.rows_per;
+    return static_cast<OutT*>(p.Yr[blk]) + (e - blk * p.rows_per * p.D);
+}
 
 template <typename OutT>
 __device__ __forceinline__ float load_out(const void* p, int64_t i) {
@@ -84,8 +95,10 @@ __global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParam
                 }
             }
         }
+        // D % 8 == 0 on this path, so the 8 outputs share one row (and one block)
+        OutT* dst0 = reduce_dst<OutT>(p, 8 * i);
         if constexpr (sizeof(OutT) == 4) {
-            float4* dst = reinterpret_cast<float4*>(p.Y) + 2 * i;
+            float4* dst = reinterpret_cast<float4*>(dst0);
             __stcs(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
             __stcs(dst + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
         } else {
@@ -94,7 +107,7 @@ __global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParam
             w.y = pack_bf16x2(acc[2], acc[3]);
             w.z = pack_bf16x2(acc[4], acc[5]);
             w.w = pack_bf16x2(acc[6], acc[7]);
-            __stcs(reinterpret_cast<uint4*>(p.Y) + i, w);
+            __stcs(reinterpret_cast<uint4*>(dst0), w);
         }
     }
 }
@@ -108,9 +121,9 @@ __global__ void __launch_bounds__(256) block_reduce_scalar_kernel(const ReducePa
         for (int r = 1; r < p.T; ++r) acc += p.P[r][i];
         if (p.bias != nullptr) acc += load_out<OutT>(p.bias, i % p.D);
         if constexpr (sizeof(OutT) == 4) {
-            static_cast<float*>(p.Y)[i] = acc;
+            *reduce_dst<float>(p, i) = acc;
         } else {
-            static_cast<__nv_bfloat16*>(p.Y)[i] = __float2bfloat16_rn(acc);
+            *reduce_dst<__nv_bfloat16>(p, i) = __float2bfloat16_rn(acc);
         }
     }
 }
@@ -323,6 +336,81 @@ __global__ void __launch_bounds__(CE_THREADS) vocab_ce_kernel(const CEParams p) 
     }
 }
 
+// CE backward: dz[n, v] = g * (exp(z[n, v] - lse_n) - 1(v = t_n)), computed by
+// every vocab shard on its own columns from the forward's per-token result;
+// lse_n = loss_n + z[n, t_n] recovers m_n + ln S_n from the forward's loss.
+// One CTA per row; 16-byte streaming loads and stores; may run in place.
+struct CEBwdParams {
+    const float* logits;
+    const int64_t* targets;
+    const float* loss;
+    float* dlogits;
+    int64_t N, V;
+    float scale;
+    int vec;
+    int* err;
+};
+
+__device__ __forceinline__ float ce_grad(float z, float lseL, float g, bool is_t) {
+    return g * (exp2f(fmaf(z, LOG2E, -lseL)) - (is_t ? 1.f : 0.f));
+}
+
+__global__ void __launch_bounds__(256) vocab_ce_bwd_kernel(const CEBwdParams p) {
+    __shared__ float s_lse;
+    __shared__ long long s_t;
+    const int64_t row = blockIdx.x;
+    const float* z = p.logits + row * p.V;
+    float* dz = p.dlogits + row * p.V;
+    if (threadIdx.x == 0) {
+        const int64_t t = p.targets[row];
+        if (t < 0 || t >= p.V) {
+            atomicCAS(p.err, 0, (int)TPMLP_ERR_ARG);
+            s_lse = __int_as_float(0x7fc00000);
+            s_t = -1;
+        } else {
+            s_lse = p.loss[row] + z[t];
+            s_t = t;
+        }
+    }
+    __syncthreads();   // z[t] is read before any thread overwrites the row
+    const float lseL = s_lse * LOG2E;
+    const int64_t t = s_t;
+    const float g = p.scale;
+    if (p.vec) {
+        const float4* zv = reinterpret_cast<const float4*>(z);
+        float4* dv = reinterpret_cast<float4*>(dz);
+        const int64_t n4 = p.V / 4;
+        int64_t i = threadIdx.x;
+        for (; i + 3 * 256 < n4; i += 4 * 256) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = __ldcs(zv + i + u * 256);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t e = 4 * (i + u * 256);
+                float4 d;
+                d.x = ce_grad(x[u].x, lseL, g, e == t);
+                d.y = ce_grad(x[u].y, lseL, g, e + 1 == t);
+                d.z = ce_grad(x[u].z, lseL, g, e + 2 == t);
+                d.w = ce_grad(x[u].w, lseL, g, e + 3 == t);
+                __stcs(dv + i + u * 256, d);
+            }
+        }
+        for (; i < n4; i += 256) {
+            const float4 x = __ldcs(zv + i);
+            const int64_t e = 4 * i;
+            float4 d;
+            d.x = ce_grad(x.x, lseL, g, e == t);
+            d.y = ce_grad(x.y, lseL, g, e + 1 == t);
+            d.z = ce_grad(x.z, lseL, g, e + 2 == t);
+            d.w = ce_grad(x.w, lseL, g, e + 3 == t);
+            __stcs(dv + i, d);
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < p.V; i += 256) dz[i] = ce_grad(z[i], lseL, g, i == t);
+    }
+}
+
 // mean of the per-token losses, one CTA, fixed summation order, fp64 accumulator
 __global__ void __launch_bounds__(1024) mean_kernel(const float* loss, int64_t N, float* out) {
     __shared__ double red[1024];
@@ -335,6 +423,46 @@ __global__ void __launch_bounds__(1024) mean_kernel(const float* loss, int64_t N
         __syncthreads();
     }
     if (threadIdx.x == 0) *out = N > 0 ? (float)(red[0] / (double)N) : __int_as_float(0x7fc00000);
+}
+
+// ------------------------------------------------------ vocab embedding --
+// Row-split table: shard k holds rows [k Vs, (k+1) Vs). Each shard would
+// return its own row for ids in its range and zeros otherwise, and the sum
+// over shards leaves exactly the owner's row; so every token's row is copied
+// from the owning shard. One warp per token, 16-byte chunks.
+
+struct EmbParams {
+    const int64_t* ids;
+    const void* table[kMaxG];
+    void* out;
+    int64_t N, V, Vs, row_bytes;
+    int vec;
+    int* err;
+};
+
+__global__ void __launch_bounds__(256) vocab_embedding_kernel(const EmbParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t n = warp_global; n < p.N; n += nwarps) {
+        const int64_t id = p.ids[n];
+        char* dst = static_cast<char*>(p.out) + n * p.row_bytes;
+        const bool valid = id >= 0 && id < p.V;
+        if (!valid && lane == 0) atomicCAS(p.err, 0, (int)TPMLP_ERR_ARG);
+        const int64_t k = valid ? id / p.Vs : 0;
+        const char* src = valid ? static_cast<const char*>(p.table[k]) + (id - k * p.Vs) * p.row_bytes
+                                : nullptr;
+        if (p.vec) {
+            const int64_t chunks = p.row_bytes / 16;
+            for (int64_t c = lane; c < chunks; c += 32) {
+                const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(src) + c)
+                                      : make_uint4(0, 0, 0, 0);
+                __stcs(reinterpret_cast<uint4*>(dst) + c, v);
+            }
+        } else {
+            for (int64_t c = lane; c < p.row_bytes; c += 32) dst[c] = valid ? src[c] : 0;
+        }
+    }
 }
 
 // ------------------------------------------------------------- self test --
@@ -357,10 +485,20 @@ __global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
 }  // namespace
 
 tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const float* const* P,
-                              const void* bias, void* Y, cudaStream_t s, const char* name) {
+                              const void* bias, void* Y, cudaStream_t s, const char* name,
+                              void* const* Y_rows) {
     if (N == 0) return TPMLP_OK;
     ReduceParams kp{};
-    bool vec = (D % 8 == 0) && aligned16(Y) && (bias == nullptr || aligned16(bias));
+    bool vec = (D % 8 == 0) && (bias == nullptr || aligned16(bias));
+    if (Y_rows != nullptr) {
+        kp.rows_per = N / T;
+        for (int r = 0; r < T; ++r) {
+            kp.Yr[r] = Y_rows[r];
+            vec = vec && aligned16(Y_rows[r]);
+        }
+    } else {
+        vec = vec && aligned16(Y);
+    }
     for (int r = 0; r < T; ++r) {
         kp.P[r] = P[r];
         vec = vec && aligned16(P[r]);
@@ -432,6 +570,57 @@ tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
     if (loss_mean != nullptr) {
         LaunchScope ls("vocab_ce_mean", s);
         mean_kernel<<<1, 1024, 0, s>>>(loss, N, loss_mean);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status run_vocab_ce_backward(int64_t N, int64_t V, const float* logits,
+                                   const int64_t* targets, const float* loss, float grad_scale,
+                                   float* dlogits, cudaStream_t s) {
+    if (N == 0) return TPMLP_OK;
+    CEBwdParams kp{};
+    kp.logits = logits;
+    kp.targets = targets;
+    kp.loss = loss;
+    kp.dlogits = dlogits;
+    kp.N = N;
+    kp.V = V;
+    kp.scale = grad_scale;
+    kp.vec = (V % 4 == 0) && aligned16(logits) && aligned16(dlogits);
+    kp.err = device_error_word();
+    if (kp.err == nullptr) return TPMLP_ERR_CUDA;
+    {
+        LaunchScope ls("vocab_ce_bwd", s);
+        vocab_ce_bwd_kernel<<<(unsigned)N, 256, 0, s>>>(kp);
+    }
+    return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status run_vocab_embedding(int f32, int64_t N, int64_t V, int64_t H, int T,
+                                 const int64_t* ids, const void* const* table, void* out,
+                                 cudaStream_t s) {
+    if (N == 0) return TPMLP_OK;
+    EmbParams kp{};
+    kp.ids = ids;
+    kp.out = out;
+    kp.N = N;
+    kp.V = V;
+    kp.Vs = V / T;
+    kp.row_bytes = H * (f32 ? 4 : 2);
+    bool vec = kp.row_bytes % 16 == 0 && aligned16(out);
+    for (int k = 0; k < T; ++k) {
+        kp.table[k] = table[k];
+        vec = vec && aligned16(table[k]);
+    }
+    kp.vec = vec;
+    kp.err = device_error_word();
+    if (kp.err == nullptr) return TPMLP_ERR_CUDA;
+    const int64_t max_grid = (int64_t)device_sm_count() * 8;
+    int64_t grid = (N + 7) / 8;            // 8 warps per CTA, one token each
+    if (grid > max_grid) grid = max_grid;
+    {
+        LaunchScope ls("vocab_embedding", s);
+        vocab_embedding_kernel<<<(unsigned)grid, 256, 0, s>>>(kp);
     }
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }

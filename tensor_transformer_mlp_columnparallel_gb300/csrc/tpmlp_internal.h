@@ -26,6 +26,9 @@ struct EpiArgs {
     void* C[kMaxG];            // per group (FOLD: group 0 only)
     const void* bias[kMaxG];   // per output column, compute element type; NULL: none
     void* aux[kMaxG];          // Z (compute element type), see EpiKind
+    // > 0: C is split by rows into blocks of row_shard rows, block i at C[i]
+    // (the reduce-scatter output of the block end); 0: C[g] as above
+    int64_t row_shard;
 };
 
 // A batch of G GEMMs of identical shape, C_g[M, N] = A_g[M, K] B_g[K, N], or,
@@ -54,15 +57,24 @@ tpmlp_status run_gemm_tc(const GemmProblem& p, cudaStream_t s);
 // fp32 inputs on CUDA cores (exact fp32 FMA, no TF32).
 tpmlp_status run_gemm_simt(const GemmProblem& p, cudaStream_t s);
 
-// Y = sum_r P[r] + bias, fp32 sum in shard order, output fp32 or bf16.
+// Y = sum_r P[r] + bias, fp32 sum in shard order, output fp32 or bf16. With
+// Y_rows != NULL the result is scattered by rows: rows [i*N/T, (i+1)*N/T) to
+// Y_rows[i] (reduce-scatter); otherwise it goes to Y.
 tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const float* const* P,
-                              const void* bias, void* Y, cudaStream_t s, const char* name);
+                              const void* bias, void* Y, cudaStream_t s, const char* name,
+                              void* const* Y_rows = nullptr);
+tpmlp_status run_vocab_embedding(int f32, int64_t N, int64_t V, int64_t H, int T,
+                                 const int64_t* ids, const void* const* table, void* out,
+                                 cudaStream_t s);
 // out_g[c] = sum_r in_g[r * ld + c] for G groups (bias gradients).
 tpmlp_status run_colsum(int f32, int64_t rows, int64_t cols, int64_t ld, int G,
                         const void* const* in, void* const* out, cudaStream_t s);
 tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
                           const int64_t* targets, float* loss, float* loss_mean, int32_t* argmax,
                           int32_t* owner, cudaStream_t s);
+tpmlp_status run_vocab_ce_backward(int64_t N, int64_t V, const float* logits,
+                                   const int64_t* targets, const float* loss, float grad_scale,
+                                   float* dlogits, cudaStream_t s);
 tpmlp_status run_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
 
 // ---- services of the API translation unit --------------------------------

@@ -328,3 +328,97 @@ def test_oracle_package_does_not_import_the_product():
         src = open(mod.__file__).read()
         assert "tensor_transformer_mlp_columnparallel_gb300" not in src
     del sys
+
+
+# ---------------------------------------------------------------------------
+# Vocab-parallel cross-entropy backward
+# ---------------------------------------------------------------------------
+
+def test_ce_backward_matches_torch_autograd():
+    g = torch.Generator().manual_seed(5)
+    z = (torch.randn(13, 40, generator=g, dtype=torch.float64) * 2.0).requires_grad_(True)
+    t = torch.randint(0, 40, (13,), generator=g)
+    torch.nn.functional.cross_entropy(z, t).backward()      # mean over tokens
+    ours = oce.vocab_ce_backward(z.detach(), t, 1.0 / 13)
+    np.testing.assert_allclose(ours, z.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_ce_backward_matches_finite_differences_of_the_forward():
+    rng = np.random.default_rng(3)
+    z = rng.standard_normal((3, 10)) * 1.5
+    t = np.array([2, 9, 0])
+    h = 1e-6
+    num = np.zeros_like(z)
+    for i in range(z.shape[0]):
+        for j in range(z.shape[1]):
+            zp, zm = z.copy(), z.copy()
+            zp[i, j] += h
+            zm[i, j] -= h
+            num[i, j] = (oce.vocab_ce(zp, t, 2)["loss"].sum() - oce.vocab_ce(zm, t, 2)["loss"].sum()) / (2 * h)
+    np.testing.assert_allclose(oce.vocab_ce_backward(z, t, 1.0), num, rtol=1e-6, atol=1e-8)
+
+
+def test_ce_backward_closed_forms_and_invariants():
+    V = 64
+    z = np.full((4, V), -0.75)
+    t = np.array([0, 5, 63, 17])
+    d = oce.vocab_ce_backward(z, t, 0.5)
+    expect = np.full((4, V), 0.5 / V)
+    expect[np.arange(4), t] -= 0.5
+    np.testing.assert_allclose(d, expect, rtol=0, atol=1e-15)
+    rng = np.random.default_rng(1)
+    z = rng.standard_normal((20, 33)) * 3
+    t = rng.integers(0, 33, 20)
+    d = oce.vocab_ce_backward(z, t, 1.0)
+    np.testing.assert_allclose(d.sum(axis=1), 0.0, atol=1e-13)       # rows of softmax - onehot sum to 0
+    assert np.all(d[np.arange(20), t] < 0) and np.all(np.delete(d.ravel(), t + 33 * np.arange(20)) > 0)
+
+
+@pytest.mark.parametrize("T", [1, 4, 11])
+def test_ce_backward_sharded_equals_one_shot(T):
+    rng = np.random.default_rng(T)
+    z = rng.standard_normal((7, 44)) * 2
+    t = rng.integers(0, 44, 7)
+    np.testing.assert_allclose(osh.vocab_ce_backward_sharded(z, t, T, 0.25),
+                               oce.vocab_ce_backward(z, t, 0.25), rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Reduce-scatter block end and vocab-parallel embedding
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_reduce_scatter_blocks_concatenate_to_the_all_reduce(T):
+    inp = gen_integer_mlp(N=8 * T, D=16, F=32, T=T, dtype="f32", bias=True, seed=19)
+    sh = osh.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "relu", T)
+    blocks = osh.block_reduce_scatter(sh["P"], inp.b2, T)
+    assert len(blocks) == T and all(b.shape == (8, 16) for b in blocks)
+    np.testing.assert_array_equal(np.concatenate(blocks, axis=0), sh["Y"])
+    full = omlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "relu")["Y"]
+    np.testing.assert_array_equal(np.concatenate(blocks, axis=0), full)
+
+
+def test_reduce_scatter_rejects_ragged_token_counts():
+    with pytest.raises(ValueError):
+        osh.block_reduce_scatter([np.zeros((5, 4))], None, 2)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_embedding_sharded_equals_gather(T):
+    from oracle import embedding as oemb
+    rng = np.random.default_rng(T)
+    E = rng.standard_normal((64, 12))
+    ids = rng.integers(0, 64, 40)
+    out = oemb.vocab_embedding(ids, E)
+    np.testing.assert_array_equal(out, E[ids])                  # the definition, by brute force
+    np.testing.assert_array_equal(osh.vocab_embedding_sharded(ids, E, T), out)
+
+
+def test_embedding_out_of_range_ids_give_zero_rows():
+    from oracle import embedding as oemb
+    E = np.arange(24, dtype=float).reshape(8, 3) + 1
+    ids = np.array([0, 8, -1, 7])
+    out = oemb.vocab_embedding(ids, E)
+    np.testing.assert_array_equal(out[[1, 2]], 0.0)
+    np.testing.assert_array_equal(out[[0, 3]], E[[0, 7]])
+    np.testing.assert_array_equal(osh.vocab_embedding_sharded(ids, E, 4), out)
