@@ -413,6 +413,33 @@ def secondary(dev, stream, steps, pk):
             out[f"{name}_{mode}"] = rec
         del fb
         torch.cuda.empty_cache()
+    # gated (SwiGLU) block, N=4096 D=4096 F=16384 T=4: gate and up as one dual
+    # GEMM per shard, then the split-K down projection
+    Ns, Ds, Fg, Tg = 4096, 4096, 16384, 4
+    gs = torch.Generator(device=dev)
+    gs.manual_seed(0)
+    Xg = torch.randn(Ns, Ds, generator=gs, device=dev).to(torch.bfloat16)
+    mk = lambda r, c: (torch.randn(r, c, generator=gs, device=dev) * 0.02).to(torch.bfloat16)
+    Wg = [mk(Ds, Fg // Tg) for _ in range(Tg)]
+    Wu = [mk(Ds, Fg // Tg) for _ in range(Tg)]
+    Wd = [mk(Fg // Tg, Ds) for _ in range(Tg)]
+    Yg = torch.empty(Ns, Ds, dtype=torch.bfloat16, device=dev)
+    Hg = [torch.empty(Ns, Fg // Tg, dtype=torch.bfloat16, device=dev) for _ in range(Tg)]
+    fn = lambda: tp.tpmlp_swiglu_forward(Xg, Wg, Wu, Wd, Yg, Hg, None, None, "splitk", None)
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    ms_s = timed(fn, steps, 3, 1, dev, stream)
+    tp.tpmlp_timing_enable(False)
+    t = tp.tpmlp_timing_read()
+    sflops = 6.0 * Ns * Ds * Fg
+    out["swiglu_bf16_n4096_d4096_f16384_t4_splitk"] = {
+        "TFLOP/s": sflops * steps / (ms_s * 1e-3) / 1e12, "ms_per_forward": ms_s / steps,
+        "kernels": kernel_table(t, ms_s),
+        "roofline": {"bound": "tensor", "achieved": sflops * steps / (ms_s * 1e-3) / 1e12,
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": sflops * steps / (ms_s * 1e-3) / 1e12 / pk["bf16_tflops_sustained"]}}
+    del Xg, Wg, Wu, Wd, Yg, Hg
+    torch.cuda.empty_cache()
     # the PARTIALS variant of the same fwd+bwd step: T fp32 partials + block reduce
     cfg = MLP_CONFIGS[WORKLOAD]
     blk = Block(cfg, "partials", dev)

@@ -94,6 +94,22 @@ tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int 
                            void* const* H, void* const* Z, tpmlp_reduce_mode mode,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Gated (SwiGLU) form of the block (§08): gate and up projections split by
+ * the SAME columns so every shard holds matching channels, the down
+ * projection by the matching rows:
+ *   G^(r) = X Wg^(r), U^(r) = X Wu^(r), H^(r) = SiLU(G^(r)) * U^(r),
+ *   Y = sum_r H^(r) Wd^(r)        SiLU(z) = z / (1 + exp(-z))
+ * The gate and up products of a shard run as ONE GEMM whose tiles carry both
+ * accumulators, and the epilogue forms H directly.
+ *   X   [N, D];  Wg, Wu  T x [D, F/T];  Wd  T x [F/T, D]
+ *   Y   [N, D] out;  H  T x [N, F/T] out;  G, U  T x [N, F/T] out, or NULL
+ * No biases. Block end, workspace and errors as tpmlp_forward. */
+tpmlp_status tpmlp_swiglu_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                  const void* X, const void* const* Wg, const void* const* Wu,
+                                  const void* const* Wd, void* Y, void* const* H, void* const* G,
+                                  void* const* U, tpmlp_reduce_mode mode, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Backward of one block (§06), for upstream gradient dY [N, D].
  *   inputs: X, W1 (T x [D, F/T]), W2 (T x [F/T, D]), H and Z (T x [N, F/T],
  *           as written by tpmlp_forward), dY [N, D]

@@ -18,6 +18,8 @@ What it computes (plain definitions, no blocking, fusion or reordering):
   over tokens, argmax per token and the shard that owns each target
   (page "unpurerationalist ... 3.4 TP for Embedding", LM head bullets;
   Megatron TP chapter §7.8).
+- ``mlp.swiglu_forward``: G = X Wg, U = X Wu, H = SiLU(G) * U, Y = H Wd
+  (same page, §08 gated MLP).
 - ``ce.vocab_ce_backward``: grad_scale * (softmax(z) - onehot(t)) (course
   notes §3.6.4).
 - ``embedding.vocab_embedding``: out[n] = E[ids[n]] (textbook §4.2.3, course

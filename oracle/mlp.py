@@ -119,3 +119,19 @@ def backward_hidden_units(X, W1, b1, W2, dY, kind, fidx):
     b1s = None if b1 is None else as_f64(b1)[fidx]
     g = backward(X, W1s, b1s, W2s, dY, kind)
     return {"dW1": g["dW1"], "dW2": g["dW2"], "db1": g["db1"]}
+
+
+def silu(z):
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_forward(X, Wg, Wu, Wd):
+    """Gated MLP of page "一层 MLP 太宽而放不下时怎样切？" §08:
+    G = X Wg, U = X Wu, H = SiLU(G) * U, Y = H Wd, with Wg, Wu [D, F] and
+    Wd [F, D] unsharded. SiLU(z) = z / (1 + exp(-z))."""
+    X, Wg, Wu, Wd = as_f64(X), as_f64(Wg), as_f64(Wu), as_f64(Wd)
+    G = X @ Wg
+    U = X @ Wu
+    H = silu(G) * U
+    return {"G": G, "U": U, "H": H, "Y": H @ Wd}

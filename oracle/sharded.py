@@ -172,3 +172,23 @@ def vocab_ce_backward_sharded(logits, targets, T, grad_scale):
                 dk[n, t[n] - k * Vs] -= 1.0
         parts.append(grad_scale * dk)
     return np.concatenate(parts, axis=1)
+
+
+def swiglu_forward_sharded(X, Wg, Wu, Wd, T, up_shard_order=None):
+    """Gate and up split by the SAME columns (§08): shard r computes
+    H^(r) = SiLU(X Wg^(r)) * (X Wu^(r)) and P^(r) = H^(r) Wd^(r); Y = sum_r P^(r).
+    `up_shard_order` plants the mistake the page warns about (up shards in a
+    different order than gate shards): shapes stay valid, channels misalign."""
+    from .mlp import silu
+    X = as_f64(X)
+    Wgs, Wus, Wds = split_columns(Wg, T), split_columns(Wu, T), split_rows(Wd, T)
+    order = list(range(T)) if up_shard_order is None else list(up_shard_order)
+    H, P = [], []
+    for r in range(T):
+        Hr = silu(X @ Wgs[r]) * (X @ Wus[order[r]])
+        H.append(Hr)
+        P.append(Hr @ Wds[r])
+    Y = P[0].copy()
+    for r in range(1, T):
+        Y = Y + P[r]
+    return {"H": H, "P": P, "Y": Y}

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     tpmlp_launch_count,
     tpmlp_selftest_wait_timeout,
     tpmlp_set_wait_timeout_ns,
+    tpmlp_swiglu_forward,
     tpmlp_timing_enable,
     tpmlp_timing_read,
     tpmlp_timing_reset,
@@ -132,3 +133,18 @@ def vocab_embedding(ids: torch.Tensor, table: Sequence[torch.Tensor]):
     out = torch.empty((ids.shape[0], table[0].shape[1]), dtype=table[0].dtype, device=ids.device)
     tpmlp_vocab_embedding(ids, list(table), out)
     return out
+
+
+def swiglu_forward(X, Wg, Wu, Wd, mode: str = "splitk", save_gate_up: bool = False):
+    """Gated MLP forward; returns (Y, H list, G list or None, U list or None)."""
+    T = len(Wg)
+    N, D = X.shape
+    Fs = Wg[0].shape[1]
+    dev, dt = X.device, X.dtype
+    Y = torch.empty((N, D), dtype=dt, device=dev)
+    H = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)]
+    G = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_gate_up else None
+    U = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_gate_up else None
+    ws = _workspace(tpmlp_workspace_bytes(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
+    tpmlp_swiglu_forward(X, list(Wg), list(Wu), list(Wd), Y, H, G, U, mode, ws)
+    return Y, H, G, U

@@ -49,6 +49,8 @@ _SIGNATURES = {
                              _PP, _PP, _int, _vp, ctypes.c_size_t, _vp]),
     "tpmlp_forward_noalloc": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _vp,
                                      _vp, _PP, _PP, _vp]),
+    "tpmlp_swiglu_forward": (_int, [_int, _i64, _i64, _i64, _int, _vp, _PP, _PP, _PP, _vp, _PP, _PP,
+                                    _PP, _int, _vp, ctypes.c_size_t, _vp]),
     "tpmlp_backward": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp, _PP, _PP, _PP, _PP, _vp,
                               _vp, _PP, _PP, _PP, _vp, _int, _vp, ctypes.c_size_t, _vp]),
     "tpmlp_block_reduce": (_int, [_int, _i64, _i64, _int, _PP, _vp, _vp, _vp]),
@@ -173,6 +175,18 @@ def tpmlp_forward_noalloc(X, W1, b1, W2, b2, Y, H, Z, act: str):
     _check(lib().tpmlp_forward_noalloc(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X),
                                        _ptrs(W1), _ptrs(b1), _ptrs(W2), _ptr(b2), _ptr(Y),
                                        _ptrs(H), _ptrs(Z), _stream(X)))
+
+
+def tpmlp_swiglu_forward(X, Wg, Wu, Wd, Y, H, G, U, mode: str, workspace=None):
+    """Gated block: H^(r) = SiLU(X Wg[r]) * (X Wu[r]), Y = sum_r H^(r) Wd[r]."""
+    T = len(Wg)
+    N, D = X.shape
+    Fs = Wg[0].shape[1]
+    _require([X, Y, workspace, *Wg, *Wu, *Wd, *H, *(G or []), *(U or [])], X.device, None)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tpmlp_swiglu_forward(_dtype_code(X), N, D, Fs * T, T, _ptr(X), _ptrs(Wg),
+                                      _ptrs(Wu), _ptrs(Wd), _ptr(Y), _ptrs(H), _ptrs(G), _ptrs(U),
+                                      MODE[mode], _ptr(workspace), ws_bytes, _stream(X)))
 
 
 def tpmlp_backward(X, W1, W2, H, Z, dY, dX, dW1, dW2, db1, db2, act: str, mode: str, workspace):

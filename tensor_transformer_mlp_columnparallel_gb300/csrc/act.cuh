@@ -26,6 +26,9 @@ __device__ __forceinline__ float act_grad(int act, float z) {
     return fmaf(0.5f * z * (1.f - t * t), du, 0.5f * (1.f + t));
 }
 
+// SiLU(z) = z / (1 + exp(-z)), the gate nonlinearity of the gated MLP.
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

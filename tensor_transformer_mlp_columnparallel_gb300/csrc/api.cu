@@ -210,6 +210,53 @@ size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, 
     return (size_t)-1;
 }
 
+// Row shards and the block-end sum (§02-§05): Y = sum_r H^(r) W2^(r) + b2, into
+// Y or, with Y_rows, row block r of Y into Y_rows[r].
+static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int Fs,
+                              const void* const* H, const void* const* W2, const void* b2,
+                              void* Y, void* const* Y_rows, tpmlp_reduce_mode mode,
+                              void* workspace, cudaStream_t s) {
+    const int f32 = dt == TPMLP_BF16 ? 0 : 1;
+    if (mode == TPMLP_REDUCE_PARTIALS) {
+        const size_t stride = round256((size_t)N * D * 4);
+        const float* parts[kMaxG];
+        GemmProblem row = problem((int)N, (int)D, Fs, T, 0, Fs, 0, D, 1, "row_gemm_partials");
+        row.epi.kind = EPI_STORE;
+        row.epi.out_f32 = 1;
+        row.epi.ldc = D;
+        for (int r = 0; r < T; ++r) {
+            float* pr = reinterpret_cast<float*>(static_cast<char*>(workspace) + r * stride);
+            row.A[r] = H[r];
+            row.B[r] = W2[r];
+            row.epi.C[r] = pr;
+            parts[r] = pr;
+        }
+        TPMLP_TRY(run_gemm(dt, row, s));
+        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s,
+                                   Y_rows ? "block_reduce_scatter_bias" : "block_reduce_bias",
+                                   Y_rows));
+    } else {
+        GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1,
+                                  Y_rows ? "row_gemm_splitk_bias_scatter" : "row_gemm_splitk_bias");
+        row.epi.kind = EPI_STORE;
+        row.epi.out_f32 = f32;
+        row.epi.ldc = D;
+        row.epi.bias[0] = b2;
+        if (Y_rows != nullptr) {
+            row.epi.row_shard = N / T;
+            for (int r = 0; r < T; ++r) row.epi.C[r] = Y_rows[r];
+        } else {
+            row.epi.C[0] = Y;
+        }
+        for (int r = 0; r < T; ++r) {
+            row.A[r] = H[r];
+            row.B[r] = W2[r];
+        }
+        TPMLP_TRY(run_gemm(dt, row, s));
+    }
+    return TPMLP_OK;
+}
+
 // The forward's steps; the block end writes Y, or, with Y_rows, row block r
 // of Y to Y_rows[r] (reduce-scatter).
 static tpmlp_status forward_impl(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
@@ -261,44 +308,8 @@ static tpmlp_status forward_impl(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F
     TPMLP_TRY(run_gemm(dt, col, s));
 
     // 2. row shards and the block-end sum
-    if (mode == TPMLP_REDUCE_PARTIALS) {
-        const size_t stride = round256((size_t)N * D * 4);
-        const float* parts[kMaxG];
-        GemmProblem row = problem((int)N, (int)D, Fs, T, 0, Fs, 0, D, 1, "row_gemm_partials");
-        row.epi.kind = EPI_STORE;
-        row.epi.out_f32 = 1;
-        row.epi.ldc = D;
-        for (int r = 0; r < T; ++r) {
-            float* pr = reinterpret_cast<float*>(static_cast<char*>(workspace) + r * stride);
-            row.A[r] = H[r];
-            row.B[r] = W2[r];
-            row.epi.C[r] = pr;
-            parts[r] = pr;
-        }
-        TPMLP_TRY(run_gemm(dt, row, s));
-        TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s,
-                                   Y_rows ? "block_reduce_scatter_bias" : "block_reduce_bias",
-                                   Y_rows));
-    } else {
-        GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1,
-                                  Y_rows ? "row_gemm_splitk_bias_scatter" : "row_gemm_splitk_bias");
-        row.epi.kind = EPI_STORE;
-        row.epi.out_f32 = f32;
-        row.epi.ldc = D;
-        row.epi.bias[0] = b2;
-        if (Y_rows != nullptr) {
-            row.epi.row_shard = N / T;
-            for (int r = 0; r < T; ++r) row.epi.C[r] = Y_rows[r];
-        } else {
-            row.epi.C[0] = Y;
-        }
-        for (int r = 0; r < T; ++r) {
-            row.A[r] = H[r];
-            row.B[r] = W2[r];
-        }
-        TPMLP_TRY(run_gemm(dt, row, s));
-    }
-    return TPMLP_OK;
+    return block_end(dt, N, D, T, Fs, reinterpret_cast<const void* const*>(H), W2, b2, Y, Y_rows,
+                     mode, workspace, s);
 }
 
 tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
@@ -319,6 +330,52 @@ tpmlp_status tpmlp_forward_reduce_scatter(tpmlp_dtype dt, int64_t N, int64_t D, 
     if (Y_rows == nullptr) return TPMLP_ERR_ARG;
     return forward_impl(dt, N, D, F, T, act, X, W1, b1, W2, b2, nullptr, Y_rows, H, Z, mode,
                         workspace, workspace_bytes, stream);
+}
+
+tpmlp_status tpmlp_swiglu_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
+                                  const void* X, const void* const* Wg, const void* const* Wu,
+                                  const void* const* Wd, void* Y, void* const* H, void* const* G,
+                                  void* const* U, tpmlp_reduce_mode mode, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    TPMLP_TRY(check_dims(dt, N, D, F, T, TPMLP_ACT_RELU));
+    if (mode != TPMLP_REDUCE_PARTIALS && mode != TPMLP_REDUCE_SPLITK) return TPMLP_ERR_ARG;
+    if (N == 0) return TPMLP_OK;
+    const bool bf = dt == TPMLP_BF16;
+    TPMLP_TRY(check_ptr(X, bf));
+    TPMLP_TRY(check_ptr(Y, bf));
+    TPMLP_TRY(check_shards(Wg, T, bf));
+    TPMLP_TRY(check_shards(Wu, T, bf));
+    TPMLP_TRY(check_shards(Wd, T, bf));
+    TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(H), T, bf));
+    if (G != nullptr) TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(G), T, bf));
+    if (U != nullptr) TPMLP_TRY(check_shards(reinterpret_cast<const void* const*>(U), T, bf));
+    const size_t need = tpmlp_workspace_bytes(TPMLP_OP_FORWARD, dt, N, D, F, T, mode);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need) return TPMLP_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Fs = (int)(F / T);
+    // 1. gate and up of shard r over the SAME columns, one dual GEMM:
+    //    G^(r) = X Wg^(r), U^(r) = X Wu^(r), H^(r) = SiLU(G^(r)) * U^(r)
+    GemmProblem col = problem((int)N, Fs, (int)D, T, 0, D, 0, Fs, 1, "col_gemm_swiglu");
+    col.dual = 1;
+    col.epi.kind = EPI_SWIGLU;
+    col.epi.out_f32 = bf ? 0 : 1;
+    col.epi.ldc = Fs;
+    col.epi.ldaux = Fs;
+    for (int r = 0; r < T; ++r) {
+        col.A[r] = X;
+        col.B[r] = Wg[r];
+        col.B2[r] = Wu[r];
+        col.epi.C[r] = H[r];
+        col.epi.aux[r] = G ? G[r] : nullptr;
+        col.epi.aux2[r] = U ? U[r] : nullptr;
+    }
+    TPMLP_TRY(run_gemm(dt, col, s));
+    // 2. the down projection's row shards and the block-end sum, as in the plain block
+    return block_end(dt, N, D, T, Fs, reinterpret_cast<const void* const*>(H), Wd, nullptr, Y,
+                     nullptr, mode, workspace, s);
 }
 
 tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,

@@ -14,6 +14,7 @@ constexpr int TM = 64, TN = 64, TK = 16;
 struct SimtParams {
     const float* A[kMaxG];
     const float* B[kMaxG];
+    const float* B2[kMaxG];   // DUAL: the up projection
     int64_t lda, ldb;
     int M, N, K, G, fold;
     EpiArgs epi;
@@ -36,23 +37,32 @@ __device__ __forceinline__ void epi_scalar(const EpiArgs& e, int g, int m, int n
     static_cast<float*>(e.C[cg])[crow * e.ldc + n] = v;
 }
 
-template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void epi_swiglu_scalar(const EpiArgs& e, int g, int m, int n, float gv,
+                                                  float uv) {
+    if (e.aux[g] != nullptr) static_cast<float*>(e.aux[g])[(int64_t)m * e.ldaux + n] = gv;
+    if (e.aux2[g] != nullptr) static_cast<float*>(e.aux2[g])[(int64_t)m * e.ldaux + n] = uv;
+    static_cast<float*>(e.C[g])[(int64_t)m * e.ldc + n] = silu_f(gv) * uv;
+}
+
+template <bool A_MN, bool B_MN, bool DUAL>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs[TK][TN + 4];
+    __shared__ float Bs2[DUAL ? TK : 1][TN + 4];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int n0 = blockIdx.x * TN, m0 = blockIdx.y * TM;
-    float acc[4][4];
+    float acc[4][4], acc2[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[i][j] = acc2[i][j] = 0.f;
 
     const int ngroups = p.fold ? p.G : 1;
     for (int gi = 0; gi < ngroups; ++gi) {
         const int g = p.fold ? gi : (int)blockIdx.z;
         const float* A = p.A[g];
         const float* B = p.B[g];
+        const float* B2 = p.B2[g];
         for (int k0 = 0; k0 < p.K; k0 += TK) {
             for (int i = threadIdx.x; i < TM * TK; i += 256) {
                 const int mm = A_MN ? i % TM : i / TK;
@@ -71,6 +81,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
                 if (n < p.N && k < p.K)
                     v = B_MN ? B[(int64_t)k * p.ldb + n] : B[(int64_t)n * p.ldb + k];
                 Bs[kk][nn] = v;
+                if (DUAL) {
+                    float v2 = 0.f;
+                    if (n < p.N && k < p.K)
+                        v2 = B_MN ? B2[(int64_t)k * p.ldb + n] : B2[(int64_t)n * p.ldb + k];
+                    Bs2[kk][nn] = v2;
+                }
             }
             __syncthreads();
 #pragma unroll
@@ -84,6 +100,15 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                if (DUAL) {
+                    float b2[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) b2[j] = Bs2[kk][tx + 16 * j];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
+                }
             }
             __syncthreads();
         }
@@ -95,7 +120,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int n = n0 + tx + 16 * j;
-            if (m < p.M && n < p.N) epi_scalar(p.epi, g_out, m, n, acc[i][j]);
+            if (m < p.M && n < p.N) {
+                if (DUAL)
+                    epi_swiglu_scalar(p.epi, g_out, m, n, acc[i][j], acc2[i][j]);
+                else
+                    epi_scalar(p.epi, g_out, m, n, acc[i][j]);
+            }
         }
     }
 }
@@ -109,6 +139,7 @@ tpmlp_status run_gemm_simt(const GemmProblem& pr, cudaStream_t s) {
     for (int g = 0; g < pr.G; ++g) {
         kp.A[g] = static_cast<const float*>(pr.A[g]);
         kp.B[g] = static_cast<const float*>(pr.B[g]);
+        kp.B2[g] = static_cast<const float*>(pr.B2[g]);
     }
     kp.lda = pr.lda;
     kp.ldb = pr.ldb;
@@ -123,14 +154,18 @@ tpmlp_status run_gemm_simt(const GemmProblem& pr, cudaStream_t s) {
     dim3 grid((pr.N + TN - 1) / TN, gy, pr.fold ? 1 : pr.G);
     {
         LaunchScope ls(pr.name, s);
-        if (pr.a_mn && pr.b_mn)
-            simt_gemm_kernel<true, true><<<grid, 256, 0, s>>>(kp);
-        else if (pr.a_mn)
-            simt_gemm_kernel<true, false><<<grid, 256, 0, s>>>(kp);
-        else if (pr.b_mn)
-            simt_gemm_kernel<false, true><<<grid, 256, 0, s>>>(kp);
-        else
-            simt_gemm_kernel<false, false><<<grid, 256, 0, s>>>(kp);
+        if (pr.dual) {
+            if (pr.a_mn || !pr.b_mn || pr.fold) return TPMLP_ERR_ARG;   // the gated MLP's column GEMM only
+            simt_gemm_kernel<false, true, true><<<grid, 256, 0, s>>>(kp);
+        } else if (pr.a_mn && pr.b_mn) {
+            simt_gemm_kernel<true, true, false><<<grid, 256, 0, s>>>(kp);
+        } else if (pr.a_mn) {
+            simt_gemm_kernel<true, false, false><<<grid, 256, 0, s>>>(kp);
+        } else if (pr.b_mn) {
+            simt_gemm_kernel<false, true, false><<<grid, 256, 0, s>>>(kp);
+        } else {
+            simt_gemm_kernel<false, false, false><<<grid, 256, 0, s>>>(kp);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }

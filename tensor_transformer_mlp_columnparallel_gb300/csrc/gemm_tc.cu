@@ -72,12 +72,15 @@ struct Cfg {
 struct TcParams {
     CUtensorMap tmA[kMaxG];
     CUtensorMap tmB[kMaxG];
+    CUtensorMap tmB2[kMaxG];   // dual: the second B (up projection)
     int M, N, K;
     int G, fold;
     int a_mn, b_mn;
     int a_3d, b_3d;   // MN-major operand read as ONE 3-D box {64, BK, rows/64} per stage
     int m_tiles, n_tiles, k_blocks;
     int num_tiles;
+    int dual;         // tile = BN/2 outputs of A B (accumulator columns [0, BN/2)) and of
+                      // A B2 (columns [BN/2, BN)); N counts outputs
     int raster;       // tile order, see decode_tile
     int band;         // band width in tiles
     EpiArgs epi;
@@ -261,6 +264,46 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
     }
 }
 
+// Gated-MLP epilogue of one thread: 32 outputs [col0, col0 + 32) of row
+// `row` from the gate accumulators rg[] and the up accumulators ru[].
+__device__ __forceinline__ void epilogue_swiglu_chunk(const EpiArgs& e, int g, int row, int col0,
+                                                      int M, int N, const uint32_t (&rg)[32],
+                                                      const uint32_t (&ru)[32]) {
+    if (row >= M) return;
+    float gv[32], uv[32], h[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        gv[j] = __uint_as_float(rg[j]);
+        uv[j] = __uint_as_float(ru[j]);
+        h[j] = silu_f(gv[j]) * uv[j];
+    }
+    const bool full = (col0 + 32 <= N);
+    const float* srcs[3] = {gv, uv, h};
+    void* dsts[3] = {e.aux[g], e.aux2[g], e.C[g]};
+    const int64_t lds[3] = {e.ldaux, e.ldaux, e.ldc};
+#pragma unroll
+    for (int o = 0; o < 3; ++o) {
+        if (dsts[o] == nullptr) continue;
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(dsts[o]) + (int64_t)row * lds[o] + col0;
+        const float* v = srcs[o];
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+                w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+                w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+                w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+                reinterpret_cast<uint4*>(d)[q] = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N) d[j] = __float2bfloat16_rn(v[j]);
+        }
+    }
+}
+
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<BN, PAIR>;
@@ -303,6 +346,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         for (int g = 0; g < p.G; ++g) {
             prefetch_tmap(&p.tmA[g]);
             prefetch_tmap(&p.tmB[g]);
+            if (p.dual) prefetch_tmap(&p.tmB2[g]);
         }
     }
     if (warp == 1) {
@@ -369,14 +413,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         for (int j = 0; j < BM / BOX_MN; ++j)
                             load(a_dst + j * MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
                     }
-                    if (!p.b_mn) {
-                        load(b_dst, &p.tmB[gk], k0, bn0);
-                    } else if (p.b_3d) {
-                        load3(b_dst, &p.tmB[gk], 0, k0, bn0 / BOX_MN);
+                    // `rows` B rows (N index) starting at n_start from map m into dst
+                    auto load_b = [&](uint32_t dst, const CUtensorMap* m, int n_start, int rows) {
+                        if (!p.b_mn) {
+                            load(dst, m, k0, n_start);
+                        } else if (p.b_3d) {
+                            load3(dst, m, 0, k0, n_start / BOX_MN);
+                        } else {
+                            for (int j = 0; j < rows / BOX_MN; ++j)
+                                load(dst + j * MN_BOX_BYTES, m, n_start + j * BOX_MN, k0);
+                        }
+                    };
+                    if (!p.dual) {
+                        load_b(b_dst, &p.tmB[gk], bn0, C::B_ROWS);
+                    } else if constexpr (PAIR) {
+                        // the even CTA stages the gate rows, the odd CTA the up rows
+                        load_b(b_dst, rank == 0 ? &p.tmB[gk] : &p.tmB2[gk], n0 / 2, BN / 2);
                     } else {
-#pragma unroll
-                        for (int j = 0; j < C::B_ROWS / BOX_MN; ++j)
-                            load(b_dst + j * MN_BOX_BYTES, &p.tmB[gk], bn0 + j * BOX_MN, k0);
+                        load_b(b_dst, &p.tmB[gk], n0 / 2, BN / 2);
+                        load_b(b_dst + (BN / 2) * BK * 2, &p.tmB2[gk], n0 / 2, BN / 2);
                     }
                     ++issued;
                     if (++s == C::STAGES) {
@@ -491,13 +546,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const int row = m0 + (int)rank * BM + quarter * 32 + lane;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            for (int c = 0; c < BN; c += 32) {
-                if (n0 + c >= p.N) break;
-                uint32_t r[32];
-                __syncwarp();
-                tmem_ld_32cols(tbase + (uint32_t)c, r);
-                tmem_ld_wait();
-                epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+            if (!p.dual) {
+                for (int c = 0; c < BN; c += 32) {
+                    if (n0 + c >= p.N) break;
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld_32cols(tbase + (uint32_t)c, r);
+                    tmem_ld_wait();
+                    epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                }
+            } else {
+                const int n0o = n0 / 2;
+                for (int c = 0; c < BN / 2; c += 32) {
+                    if (n0o + c >= p.N) break;
+                    uint32_t rg[32], ru[32];
+                    __syncwarp();
+                    tmem_ld_32cols(tbase + (uint32_t)c, rg);
+                    tmem_ld_32cols(tbase + (uint32_t)(BN / 2 + c), ru);
+                    tmem_ld_wait();
+                    epilogue_swiglu_chunk(p.epi, g, row, n0o + c, p.M, p.N, rg, ru);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -590,22 +658,31 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
     const int G = pr.G;
     // MN-major operands whose MN extent is a multiple of 64 use one 3-D box per
     // stage; if the driver refuses that map, the 2-D boxes are used instead
+    // B rows staged per map: half the tile's N for a dual GEMM
+    const int b_rows = pr.dual ? BN / 2 : C::B_ROWS;
     kp.a_3d = pr.a_mn && pr.M % BOX_MN == 0;
     kp.b_3d = pr.b_mn && pr.N % BOX_MN == 0;
     for (int g = 0; g < G && kp.a_3d; ++g)
         kp.a_3d = make_map_mn_chunks(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BM);
-    for (int g = 0; g < G && kp.b_3d; ++g)
-        kp.b_3d = make_map_mn_chunks(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, C::B_ROWS);
+    for (int g = 0; g < G && kp.b_3d; ++g) {
+        kp.b_3d = make_map_mn_chunks(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, b_rows);
+        if (kp.b_3d && pr.dual)
+            kp.b_3d = make_map_mn_chunks(&kp.tmB2[g], pr.B2[g], pr.N, pr.K, pr.ldb, b_rows);
+    }
     for (int g = 0; g < G; ++g) {
         bool ok = true;
         if (!pr.a_mn)
             ok = make_map(&kp.tmA[g], pr.A[g], pr.K, pr.M, pr.lda, BK, BM);
         else if (!kp.a_3d)
             ok = make_map(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BOX_MN, BK);
-        if (!pr.b_mn)
-            ok = ok && make_map(&kp.tmB[g], pr.B[g], pr.K, pr.N, pr.ldb, BK, C::B_ROWS);
-        else if (!kp.b_3d)
-            ok = ok && make_map(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, BOX_MN, BK);
+        for (int d = 0; d < (pr.dual ? 2 : 1); ++d) {
+            CUtensorMap* m = d == 0 ? &kp.tmB[g] : &kp.tmB2[g];
+            const void* b = d == 0 ? pr.B[g] : pr.B2[g];
+            if (!pr.b_mn)
+                ok = ok && make_map(m, b, pr.K, pr.N, pr.ldb, BK, b_rows);
+            else if (!kp.b_3d)
+                ok = ok && make_map(m, b, pr.N, pr.K, pr.ldb, BOX_MN, BK);
+        }
         if (!ok) return TPMLP_ERR_CUDA;
     }
     kp.M = pr.M;
@@ -616,7 +693,8 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
     kp.a_mn = pr.a_mn;
     kp.b_mn = pr.b_mn;
     kp.m_tiles = (pr.M + C::TILE_M - 1) / C::TILE_M;
-    kp.n_tiles = (pr.N + BN - 1) / BN;
+    kp.dual = pr.dual;
+    kp.n_tiles = pr.dual ? (pr.N + BN / 2 - 1) / (BN / 2) : (pr.N + BN - 1) / BN;
     kp.k_blocks = (pr.K + BK - 1) / BK;
     kp.num_tiles = (pr.fold ? 1 : G) * kp.m_tiles * kp.n_tiles;
     {
@@ -707,8 +785,9 @@ tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
         const Cand& c = cands[i];
         if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
         const int64_t tile_m = c.pair ? 256 : 128;
+        const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
         const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
-                              ((pr.N + c.bn - 1) / c.bn);
+                              ((pr.N + n_out - 1) / n_out);
         const int64_t units = c.pair ? sms / 2 : sms;
         const int64_t waves = (tiles + units - 1) / units;
         const double cost = pr.M <= 64 ? (double)waves * c.bn

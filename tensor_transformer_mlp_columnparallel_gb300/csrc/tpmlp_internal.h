@@ -15,7 +15,9 @@ constexpr int kMaxG = TPMLP_MAX_SHARDS;
 //   EPI_STORE: C = v (+ bias[n])
 //   EPI_ACT:   z = v (+ bias[n]); aux = z (if aux != NULL); C = act(z)
 //   EPI_DACT:  C = v * act'(aux[m, n])
-enum EpiKind { EPI_STORE = 0, EPI_ACT = 1, EPI_DACT = 2 };
+//   EPI_SWIGLU (dual GEMMs): g, u = the two accumulators at (m, n);
+//              aux = g, aux2 = u (each if not NULL); C = SiLU(g) * u
+enum EpiKind { EPI_STORE = 0, EPI_ACT = 1, EPI_DACT = 2, EPI_SWIGLU = 3 };
 
 struct EpiArgs {
     int kind;
@@ -26,6 +28,7 @@ struct EpiArgs {
     void* C[kMaxG];            // per group (FOLD: group 0 only)
     const void* bias[kMaxG];   // per output column, compute element type; NULL: none
     void* aux[kMaxG];          // Z (compute element type), see EpiKind
+    void* aux2[kMaxG];         // U of EPI_SWIGLU
     // > 0: C is split by rows into blocks of row_shard rows, block i at C[i]
     // (the reduce-scatter output of the block end); 0: C[g] as above
     int64_t row_shard;
@@ -48,6 +51,10 @@ struct GemmProblem {
     const void* B[kMaxG];
     int64_t ldb;
     int b_mn;
+    // dual = 1: a second B (B2, same layout as B) and two products per output,
+    // A B and A B2, for the gated MLP's gate and up projections
+    int dual;
+    const void* B2[kMaxG];
     EpiArgs epi;
     const char* name;          // kernel kind, for the timing records
 };

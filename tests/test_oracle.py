@@ -422,3 +422,49 @@ def test_embedding_out_of_range_ids_give_zero_rows():
     np.testing.assert_array_equal(out[[1, 2]], 0.0)
     np.testing.assert_array_equal(out[[0, 3]], E[[0, 7]])
     np.testing.assert_array_equal(osh.vocab_embedding_sharded(ids, E, 4), out)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU gated MLP
+# ---------------------------------------------------------------------------
+
+def test_swiglu_matches_torch():
+    g = torch.Generator().manual_seed(6)
+    X = torch.randn(9, 12, generator=g, dtype=torch.float64)
+    Wg, Wu = (torch.randn(12, 20, generator=g, dtype=torch.float64) * 0.5 for _ in range(2))
+    Wd = torch.randn(20, 12, generator=g, dtype=torch.float64) * 0.5
+    ref = (torch.nn.functional.silu(X @ Wg) * (X @ Wu)) @ Wd
+    out = omlp.swiglu_forward(X, Wg, Wu, Wd)
+    np.testing.assert_allclose(out["Y"], ref.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(omlp.silu(np.array([0.0, 1.0])), [0.0, 1.0 / (1.0 + np.exp(-1.0))],
+                               rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_swiglu_same_column_split_equals_unsharded(T):
+    rng = np.random.default_rng(T)
+    X = rng.standard_normal((6, 8))
+    Wg, Wu = rng.standard_normal((8, 16)), rng.standard_normal((8, 16))
+    Wd = rng.standard_normal((16, 8))
+    full = omlp.swiglu_forward(X, Wg, Wu, Wd)
+    sh = osh.swiglu_forward_sharded(X, Wg, Wu, Wd, T)
+    assert normwise_rel_err(sh["Y"], full["Y"]) <= 1e-12
+    np.testing.assert_allclose(np.concatenate(sh["H"], axis=1), full["H"], rtol=0, atol=1e-12)
+
+
+def test_swiglu_channel_tags_detect_misaligned_up_shards():
+    """Channel tags (page §10: give gate/up recognisable channel numbers): with
+    x = [1] and Wg[0, c] = Wu[0, c] = c + 1, channel c of H is SiLU(c + 1) (c + 1).
+    Swapping the order of the up shards keeps every shape valid but moves the
+    tags, and the result no longer equals the unsharded one."""
+    F, T = 8, 2
+    X = np.ones((1, 1))
+    tags = np.arange(1, F + 1, dtype=float)[None, :]
+    Wd = np.eye(F)[:, :1] + 0.1              # any row-shardable down projection
+    full = omlp.swiglu_forward(X, tags, tags, Wd)
+    np.testing.assert_allclose(full["H"][0], omlp.silu(tags[0]) * tags[0], rtol=1e-15)
+    good = osh.swiglu_forward_sharded(X, tags, tags, Wd, T)
+    np.testing.assert_allclose(np.concatenate(good["H"], axis=1), full["H"], rtol=1e-15)
+    bad = osh.swiglu_forward_sharded(X, tags, tags, Wd, T, up_shard_order=[1, 0])
+    assert not np.allclose(np.concatenate(bad["H"], axis=1), full["H"])
+    assert normwise_rel_err(bad["Y"], full["Y"]) > TOL["bf16"]
