@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="N,D,F,T override of the fwd+bwd workload (small cases for profiling)")
+    ap.add_argument("--only-ce", type=int, default=0, metavar="TOKENS",
+                    help="time only the vocab CE forward and backward (V=128000, T=8) on TOKENS "
+                         "tokens (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -287,11 +290,14 @@ def cpu_baseline_mlp(cfg, tokens=96):
                       f"host cores), {dt:.1f} s"}
 
 
-def secondary(dev, stream, steps, pk):
+def secondary(dev, stream, steps, pk, ce_tokens=0):
+    import dataclasses
     import tensor_transformer_mlp_columnparallel_gb300 as tp
     out = {}
     # vocab-parallel CE, N = 8192, V = 128000, T = 8: logits drawn on the device
     ce = CE_CONFIGS["vocab_ce_n8192_v128000_t8"]
+    if ce_tokens:
+        ce = dataclasses.replace(ce, N=ce_tokens)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     logits = torch.randn((ce.N, ce.V), generator=g, device=dev) * ce.logit_std
@@ -332,6 +338,8 @@ def secondary(dev, stream, steps, pk):
                      "algorithmic_bytes_per_launch": bwd_bytes}}
     del logits, dlog
     torch.cuda.empty_cache()
+    if ce_tokens:
+        return out
     # block end as a reduce-scatter (T = 8 fp32 partials of [8192, 8192] -> 8 bf16
     # row blocks of [1024, 8192]); the partials exceed L2
     Tn, Nn, Dn = 8, 8192, 8192
@@ -624,8 +632,20 @@ def run_reference(args):
     }))
 
 
+def run_only_ce(args):
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    out = secondary(dev, torch.cuda.current_stream(dev), args.steps, peaks(), args.only_ce)
+    print(json.dumps({"only": "vocab_ce", "tokens": args.only_ce, "results": out}))
+
+
 def main():
     args = parse()
+    if args.only_ce:
+        run_only_ce(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
