@@ -454,11 +454,19 @@ __global__ void __launch_bounds__(256) vocab_embedding_kernel(const EmbParams p)
                                 : nullptr;
         if (p.vec) {
             const int64_t chunks = p.row_bytes / 16;
-            for (int64_t c = lane; c < chunks; c += 32) {
-                const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(src) + c)
-                                      : make_uint4(0, 0, 0, 0);
-                __stcs(reinterpret_cast<uint4*>(dst) + c, v);
+            const uint4* sv = reinterpret_cast<const uint4*>(src);
+            uint4* dv = reinterpret_cast<uint4*>(dst);
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            int64_t c = lane;
+            // four independent 16-byte loads in flight per lane
+            for (; c + 96 < chunks; c += 128) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = valid ? __ldg(sv + c + 32 * u) : zero;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) __stcs(dv + c + 32 * u, v[u]);
             }
+            for (; c < chunks; c += 32) __stcs(dv + c, valid ? __ldg(sv + c) : zero);
         } else {
             for (int64_t c = lane; c < p.row_bytes; c += 32) dst[c] = valid ? src[c] : 0;
         }
