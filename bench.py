@@ -244,12 +244,23 @@ def kernel_table(t, total_ms):
     return out
 
 
-def kernel_source_hash():
-    """sha256 over the library's CUDA sources (file name + bytes, sorted)."""
+KERNEL_FAMILIES = {
+    # kernel timing name prefix -> CUDA sources that define that kernel
+    "gemm": ("gemm_tc.cu", "ptx.cuh", "act.cuh", "tpmlp_internal.h"),
+    "hbm": ("hbm_kernels.cu", "ptx.cuh", "act.cuh", "tpmlp_internal.h"),
+}
+
+
+def kernel_family(kernel):
+    return "gemm" if "gemm" in kernel else "hbm"
+
+
+def kernel_source_hash(family="gemm"):
+    """sha256 over the CUDA sources of one kernel family (file name + bytes)."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "tensor_transformer_mlp_columnparallel_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_FAMILIES[family]:
         h.update(f.encode())
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()
@@ -258,13 +269,14 @@ def kernel_source_hash():
 def load_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/traffic.json), or None when that summary was taken on other
-    kernel sources than the ones built now."""
+    sources of the kernel's family than the ones built now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        if d.get("source_hash") != kernel_source_hash():
+        fam = kernel_family(kernel)
+        if d.get("source_hash", {}).get(fam) != kernel_source_hash(fam):
             return None
         return d["kernels"].get(kernel, {}).get("dram_bytes_per_launch")
     except Exception:
