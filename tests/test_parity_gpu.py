@@ -190,7 +190,7 @@ def test_ragged_shapes_forward_backward(mode, act, dtype):
     check_backward(inp, grads, dtype)
 
 
-@pytest.mark.parametrize("T", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("mode", MODES)
 def test_shard_count_sweep_bf16(T, mode):
     inp = gen_random_mlp(N=256, D=512, F=2048, T=T, dtype="bf16", act="gelu_tanh", bias=True, seed=T)
@@ -427,3 +427,32 @@ def test_timing_records_every_kernel_kind():
             "bias_grad_colsum"} <= names
     assert tp.tpmlp_launch_count() - before == sum(v["launches"] for v in t.values())
     assert all(v["total_ms"] > 0 for v in t.values())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", MODES)
+def test_inference_forward_without_saved_z(dtype, mode):
+    inp = gen_random_mlp(N=200, D=264, F=4 * 136, T=4, dtype=dtype, act="gelu_tanh", bias=True,
+                         seed=12, with_dy=False)
+    gp = to_gpu(inp)
+    Y, H, Z = run_forward(gp, "gelu_tanh", mode, save_z=False)
+    torch.cuda.synchronize()
+    assert Z is None
+    check_forward(inp, Y, H, None, dtype)
+
+
+def test_max_shard_count_and_beyond():
+    """T = 16 (the library's maximum) runs; T = 17 is rejected before launch."""
+    inp = gen_random_mlp(N=256, D=256, F=16 * 64, T=16, dtype="bf16", act="relu", bias=True, seed=16)
+    gp = to_gpu(inp)
+    Y, H, Z = run_forward(gp, "relu", "splitk")
+    grads = run_backward(gp, H, Z, "relu", "splitk", bias_grads=True)
+    torch.cuda.synchronize()
+    check_forward(inp, Y, H, Z, "bf16")
+    check_backward(inp, grads, "bf16")
+    W1 = gp["W1"] + [gp["W1"][0]]
+    W2 = gp["W2"] + [gp["W2"][0]]
+    H17 = H + [H[0]]
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_forward(gp["X"], W1, None, W2, None, Y, H17, None, "relu", "splitk")
+    assert e.value.status == _binding.ERR_SHAPE
