@@ -33,6 +33,9 @@
  *   tpmlp_check_device_error() reads.
  * - The library allocates no device memory. Scratch space is the caller's
  *   `workspace`; tpmlp_workspace_bytes() gives its size.
+ * - Output buffers must not overlap input buffers, each other or the
+ *   workspace (the one exception is tpmlp_vocab_ce_backward, which may run in
+ *   place); overlapping buffers give undefined results.
  * - bf16 path alignment: every pointer 16-byte aligned and D % 8 == 0,
  *   (F/T) % 8 == 0 (tensor-memory-access row pitches are multiples of 16
  *   bytes); otherwise TPMLP_ERR_ALIGN.
