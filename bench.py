@@ -80,7 +80,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -95,7 +95,7 @@ class ClockSampler:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -219,10 +219,15 @@ def max_over_ranks(x, world, dev):
     return float(t.item())
 
 
-def timed(fn, steps, warmup, world, dev, stream):
+def timed(fn, steps, warmup, world, dev, stream, reset=None):
+    """Device time (ms) of `steps` calls of fn after `warmup` untimed ones;
+    `reset` (e.g. the library's kernel-timing reset) runs between the two so
+    per-kernel tables cover the timed calls only."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if reset is not None:
+        reset()
     barrier(world)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
@@ -321,7 +326,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     fn = lambda: tp.tpmlp_vocab_ce(logits, targets, ce.T, loss, mean, amax, own)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    timed(fn, steps, 3, 1, dev, stream)
+    timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
     tp.tpmlp_timing_enable(False)
     t = tp.tpmlp_timing_read()
     k = t["vocab_ce_fwd"]
@@ -336,7 +341,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     fnb = lambda: tp.tpmlp_vocab_ce_backward(logits, targets, ce.T, loss, 1.0 / ce.N, dlog)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    timed(fnb, steps, 3, 1, dev, stream)
+    timed(fnb, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
     tp.tpmlp_timing_enable(False)
     t = tp.tpmlp_timing_read()
     k = t["vocab_ce_bwd"]
@@ -361,7 +366,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     fn = lambda: tp.tpmlp_block_reduce_scatter(parts, b2, rows_out)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    timed(fn, steps, 3, 1, dev, stream)
+    timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
     tp.tpmlp_timing_enable(False)
     k = tp.tpmlp_timing_read()["block_reduce_scatter_bias"]
     ms = k["total_ms"] / k["launches"]
@@ -412,7 +417,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
             fb.set_mode(mode)
             tp.tpmlp_timing_reset()
             tp.tpmlp_timing_enable(True)
-            ms_f = timed(fb.forward, steps, 3, 1, dev, stream)
+            ms_f = timed(fb.forward, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
             tp.tpmlp_timing_enable(False)
             t = tp.tpmlp_timing_read()
             flops = fc.fwd_flops()
@@ -448,7 +453,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     fn = lambda: tp.tpmlp_swiglu_forward(Xg, Wg, Wu, Wd, Yg, Hg, None, None, "splitk", None)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    ms_s = timed(fn, steps, 3, 1, dev, stream)
+    ms_s = timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
     tp.tpmlp_timing_enable(False)
     t = tp.tpmlp_timing_read()
     sflops = 6.0 * Ns * Ds * Fg
@@ -465,7 +470,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     blk = Block(cfg, "partials", dev)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    ms_total = timed(blk.step, max(3, steps // 2), 3, 1, dev, stream)
+    ms_total = timed(blk.step, max(3, steps // 2), 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
     tp.tpmlp_timing_enable(False)
     t = tp.tpmlp_timing_read()
     nsteps = max(3, steps // 2)
