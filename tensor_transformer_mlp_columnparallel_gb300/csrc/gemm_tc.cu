@@ -370,6 +370,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (each CTA loads its own rows) ----------------
+            // The issue loop is on the critical path (the TMA unit drains its
+            // queue quickly), so it carries its shard and K offset as counters
+            // instead of dividing the k-block index.
+            // the pair's stage is complete when BOTH CTAs' bytes landed on the
+            // even CTA's full barrier
+            const uint32_t full0 = PAIR ? mapa_shared(bar(FULL), 0) : bar(FULL);
+            const int k_group = kb_per_group * BK;   // K extent of one shard
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
@@ -379,16 +386,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
                 const int am0 = m0 + (int)rank * BM;          // this CTA's A rows
                 const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
-                for (int kb = 0; kb < kb_total; ++kb) {
-                    const int gk = p.fold ? kb / kb_per_group : g;
-                    const int k0 = (p.fold ? kb - gk * kb_per_group : kb) * BK;
+                int gk = p.fold ? 0 : g;                      // shard of this k-block
+                int k0 = 0;                                   // its K offset inside the shard
+                for (int kb = 0; kb < kb_total; ++kb, k0 += BK) {
+                    if (k0 == k_group) {   // folded K loop: next shard
+                        k0 = 0;
+                        ++gk;
+                    }
                     if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
                     }
-                    // the pair's stage is complete when BOTH CTAs' bytes landed on the
-                    // even CTA's full barrier
-                    const uint32_t fb = PAIR ? mapa_shared(bar(FULL + s), 0) : bar(FULL + s);
+                    const uint32_t fb = full0 + 8u * (uint32_t)s;
                     if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
                     const uint32_t a_dst = sA0 + s * C::A_BYTES;
                     const uint32_t b_dst = sB0 + s * C::B_BYTES;
