@@ -29,6 +29,40 @@ __device__ __forceinline__ float act_grad(int act, float z) {
 // SiLU(z) = z / (1 + exp(-z)), the gate nonlinearity of the gated MLP.
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Forms for the tensor-core epilogue, whose outputs are rounded to bf16
+// (relative step 2^-8): tanh from the hardware approximation tanh.approx.f32
+// (maximum relative error about 2^-11), and SiLU through the identity
+// sigmoid(z) = (1 + tanh(z/2)) / 2. They cut the epilogue's instruction count,
+// which matters because the epilogue warps share issue slots with the TMA
+// and MMA threads. The fp32 path keeps the tanhf / expf forms above.
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float act_fwd_bf16(int act, float z) {
+    if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
+    const float c = 0.7978845608028654f;
+    const float t = tanh_hw(c * fmaf(0.044715f * z, z * z, z));
+    const float hz = 0.5f * z;
+    return fmaf(hz, t, hz);
+}
+
+__device__ __forceinline__ float act_grad_bf16(int act, float z) {
+    if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    const float c = 0.7978845608028654f;
+    const float z2 = z * z;
+    const float t = tanh_hw(c * fmaf(0.044715f * z, z2, z));
+    const float du = c * fmaf(3.f * 0.044715f, z2, 1.f);
+    return fmaf(0.5f * z * fmaf(-t, t, 1.f), du, fmaf(0.5f, t, 0.5f));
+}
+
+__device__ __forceinline__ float silu_bf16(float z) {
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_hw(hz), hz);
+}
+
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

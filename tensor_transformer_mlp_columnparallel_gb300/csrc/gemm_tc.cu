@@ -203,7 +203,7 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
             }
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = act_fwd(e.act, v[j]);
+        for (int j = 0; j < 32; ++j) v[j] = act_fwd_bf16(e.act, v[j]);
     } else if (e.kind == EPI_DACT) {
         const __nv_bfloat16* z =
             static_cast<const __nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
@@ -216,14 +216,14 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
                 for (int h = 0; h < 4; ++h) {
                     float lo, hi;
                     unpack_bf16x2(ws[h], lo, hi);
-                    v[q * 8 + 2 * h] *= act_grad(e.act, lo);
-                    v[q * 8 + 2 * h + 1] *= act_grad(e.act, hi);
+                    v[q * 8 + 2 * h] *= act_grad_bf16(e.act, lo);
+                    v[q * 8 + 2 * h + 1] *= act_grad_bf16(e.act, hi);
                 }
             }
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < N) v[j] *= act_grad(e.act, bf2f(z[j]));
+                if (col0 + j < N) v[j] *= act_grad_bf16(e.act, bf2f(z[j]));
         }
     }
     int cg = g;
@@ -275,7 +275,7 @@ __device__ __forceinline__ void epilogue_swiglu_chunk(const EpiArgs& e, int g, i
     for (int j = 0; j < 32; ++j) {
         gv[j] = __uint_as_float(rg[j]);
         uv[j] = __uint_as_float(ru[j]);
-        h[j] = silu_f(gv[j]) * uv[j];
+        h[j] = silu_bf16(gv[j]) * uv[j];
     }
     const bool full = (col0 + 32 <= N);
     const float* srcs[3] = {gv, uv, h};
