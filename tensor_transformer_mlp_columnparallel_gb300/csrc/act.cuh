@@ -2,7 +2,8 @@
 // ReLU: act'(0) = 0. GELU, tanh form (Hendrycks & Gimpel 2016):
 //   act(z)  = 0.5 z (1 + tanh(u)),  u = sqrt(2/pi) (z + 0.044715 z^3)
 //   act'(z) = 0.5 (1 + tanh(u)) + 0.5 z (1 - tanh(u)^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2)
-// tanh comes from CUDA's tanhf.
+// tanh comes from CUDA's tanhf (fp32 path) or from tanh.approx.f32 (bf16
+// tensor-core epilogue, the *_bf16 forms below).
 #pragma once
 #include <cuda_bf16.h>
 
