@@ -2,8 +2,8 @@
 // ReLU: act'(0) = 0. GELU, tanh form (Hendrycks & Gimpel 2016):
 //   act(z)  = 0.5 z (1 + tanh(u)),  u = sqrt(2/pi) (z + 0.044715 z^3)
 //   act'(z) = 0.5 (1 + tanh(u)) + 0.5 z (1 - tanh(u)^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2)
-// tanh comes from CUDA's tanhf (fp32 path) or from tanh.approx.f32 (bf16
-// tensor-core epilogue, the *_bf16 forms below).
+// tanh comes from CUDA's tanhf on the fp32 path; the bf16 tensor-core
+// epilogue uses the equivalent sigmoid forms below.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -31,37 +31,36 @@ __device__ __forceinline__ float act_grad(int act, float z) {
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
 // Forms for the tensor-core epilogue, whose outputs are rounded to bf16
-// (relative step 2^-8): tanh from the hardware approximation tanh.approx.f32
-// (maximum relative error about 2^-11), and SiLU through the identity
-// sigmoid(z) = (1 + tanh(z/2)) / 2. They cut the epilogue's instruction count,
-// which matters because the epilogue warps share issue slots with the TMA
-// and MMA threads. The fp32 path keeps the tanhf / expf forms above.
-__device__ __forceinline__ float tanh_hw(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
+// (relative step 2^-8). They cut the epilogue's instruction count, which
+// matters because the epilogue warps share issue slots with the TMA and MMA
+// threads, and stay relatively accurate in both tails:
+//   0.5 z (1 + tanh(u)) = z s,            s = sigmoid(2u) = 1 / (1 + e), e = exp(-2u)
+//   act'(z) = s + 2 z s (1 - s) u'(z) = s (1 + 2 z u'(z) e s)     (1 - s = e s)
+//   SiLU(z) = z / (1 + exp(-z))
+// with CUDA's __expf and __fdividef. The exponent is clamped at 80 so that
+// e, 1 + e and e s stay finite (for 2u < -80 the outputs are below 1e-33 in
+// magnitude either way). The fp32 path keeps the tanhf / expf forms above.
 __device__ __forceinline__ float act_fwd_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
     const float c = 0.7978845608028654f;
-    const float t = tanh_hw(c * fmaf(0.044715f * z, z * z, z));
-    const float hz = 0.5f * z;
-    return fmaf(hz, t, hz);
+    const float u = c * fmaf(0.044715f * z, z * z, z);
+    const float e = __expf(fminf(-2.f * u, 80.f));
+    return __fdividef(z, 1.f + e);
 }
 
 __device__ __forceinline__ float act_grad_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     const float c = 0.7978845608028654f;
     const float z2 = z * z;
-    const float t = tanh_hw(c * fmaf(0.044715f * z, z2, z));
+    const float u = c * fmaf(0.044715f * z, z2, z);
     const float du = c * fmaf(3.f * 0.044715f, z2, 1.f);
-    return fmaf(0.5f * z * fmaf(-t, t, 1.f), du, fmaf(0.5f, t, 0.5f));
+    const float e = __expf(fminf(-2.f * u, 80.f));
+    const float s = __fdividef(1.f, 1.f + e);
+    return s * fmaf(2.f * z * du, e * s, 1.f);
 }
 
 __device__ __forceinline__ float silu_bf16(float z) {
-    const float hz = 0.5f * z;
-    return fmaf(hz, tanh_hw(hz), hz);
+    return __fdividef(z, 1.f + __expf(fminf(-z, 80.f)));
 }
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
