@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     tpmlp_forward,
     tpmlp_forward_noalloc,
     tpmlp_forward_reduce_scatter,
+    tpmlp_gemm_plan,
     tpmlp_launch_count,
     tpmlp_selftest_wait_timeout,
     tpmlp_set_wait_timeout_ns,

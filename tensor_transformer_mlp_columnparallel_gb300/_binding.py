@@ -66,6 +66,8 @@ _SIGNATURES = {
     "tpmlp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "tpmlp_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "tpmlp_launch_count": (ctypes.c_int64, []),
+    "tpmlp_gemm_plan": (_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _int, _int, _int,
+                               ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "tpmlp_timing_enable": (None, [_int]),
     "tpmlp_timing_read": (_int, [ctypes.POINTER(KernelTiming), _int]),
     "tpmlp_timing_reset": (None, []),
@@ -289,6 +291,15 @@ def tpmlp_selftest_wait_timeout(timeout_ns: int, device=None):
 
 def tpmlp_launch_count() -> int:
     return int(lib().tpmlp_launch_count())
+
+
+def tpmlp_gemm_plan(M: int, N: int, K: int, G: int, fold: bool = False, dual: bool = False):
+    """Launch configuration of the bf16 tensor-core GEMM for this shape on the
+    current device: (accumulator columns, CTAs per MMA, K-split cluster size)."""
+    bn, ctas, ks = _int(0), _int(0), _int(0)
+    _check(lib().tpmlp_gemm_plan(M, N, K, G, 1 if fold else 0, 1 if dual else 0,
+                                 ctypes.byref(bn), ctypes.byref(ctas), ctypes.byref(ks)))
+    return bn.value, ctas.value, ks.value
 
 
 def tpmlp_timing_enable(on: bool):

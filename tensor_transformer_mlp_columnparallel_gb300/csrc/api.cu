@@ -571,6 +571,17 @@ tpmlp_status tpmlp_vocab_ce_backward(int64_t N, int64_t V, int T, const float* l
                                  static_cast<cudaStream_t>(stream));
 }
 
+tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, int dual, int* bn,
+                             int* mma_ctas, int* ksplit) {
+    if (bn == nullptr || mma_ctas == nullptr || ksplit == nullptr) return TPMLP_ERR_ARG;
+    const int64_t lim = 2147483647;
+    if (M < 1 || N < 1 || K < 1 || M > lim || N > lim || K > lim || G < 1 || G > TPMLP_MAX_SHARDS)
+        return TPMLP_ERR_SHAPE;
+    GemmProblem p = problem((int)M, (int)N, (int)K, G, fold ? 1 : 0, K, 0, K, 0, "plan");
+    p.dual = dual ? 1 : 0;
+    return plan_gemm_tc(p, bn, mma_ctas, ksplit);
+}
+
 const char* tpmlp_status_str(tpmlp_status s) {
     switch (s) {
         case TPMLP_OK: return "TPMLP_OK";

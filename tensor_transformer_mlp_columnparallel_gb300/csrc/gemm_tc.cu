@@ -44,6 +44,7 @@ constexpr int ACC_BUFS = 2;
 constexpr int BOX_MN = 64;        // MN extent of an MN-major box (128 bytes)
 constexpr int MN_BOX_BYTES = BOX_MN * BK * 2;   // 8 KB
 constexpr int GROUP_M = 8;        // raster band height, in M tiles
+constexpr int KSPLIT_ROWS = 64;   // rows a K-split cluster exchanges (M <= 64)
 
 // BN: accumulator columns (MMA N). PAIR: a CTA pair (cluster of 2) issues
 // cta_group::2 MMAs of M = 256; each CTA stages its own 128 rows of A and its
@@ -61,12 +62,16 @@ struct Cfg {
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 3;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
     static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
     static_assert(B_ROWS % BOX_MN == 0, "MN-major B boxes");
+    // K split across a cluster (single-CTA tiles, M <= KSPLIT_ROWS): each peer's
+    // partial accumulator rows land in the leader's freed stage memory
+    static constexpr int RED_SLOT_BYTES = KSPLIT_ROWS * BN * 4;
+    static constexpr int MAX_KSPLIT = PAIR ? 1 : 1 + (STAGES * STAGE_BYTES) / RED_SLOT_BYTES;
 };
 
 struct TcParams {
@@ -83,6 +88,8 @@ struct TcParams {
                       // A B2 (columns [BN/2, BN)); N counts outputs
     int raster;       // tile order, see decode_tile
     int band;         // band width in tiles
+    int ksplit;       // CTAs of a cluster sharing one tile's K range (single-CTA
+                      // tiles, M <= KSPLIT_ROWS, one tile per cluster); 1 = off
     EpiArgs epi;
     int* err;
     uint64_t timeout_ns;
@@ -318,15 +325,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     const uint32_t bar0 = smem_u32(bars);
     // barrier indices
     const int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = TFULL + ACC_BUFS,
-              DRAIN = TEMPTY + ACC_BUFS;
+              DRAIN = TEMPTY + ACC_BUFS, RFREE = DRAIN + 1, RFULL = DRAIN + 2;
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;      // CTA within the pair
     const bool leader = rank == 0;
-    const int first_tile = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
-    const int tile_step = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
+    // K split: CTA `krank` of a cluster of `ks` accumulates its share of the
+    // tile's k-blocks; the peers hand their partial rows to CTA 0
+    const int ks = PAIR ? 1 : p.ksplit;
+    const uint32_t krank = ks > 1 ? cluster_ctarank() : 0u;
+    const bool clustered = PAIR || ks > 1;
+    const int first_tile = clustered ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int tile_step = clustered ? (int)num_clusters_x() : (int)gridDim.x;
+    // epilogue warps holding rows that a K split exchanges (rows < min(M, 64))
+    const int red_warps = (min(p.M, KSPLIT_ROWS) + 31) / 32;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -338,6 +352,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             mbar_init(bar(TEMPTY + a), 4 * C::CTAS);   // every epilogue warp of the pair
         }
         mbar_init(bar(DRAIN), 1);
+        mbar_init(bar(RFREE), 1);                                  // leader: stages free
+        mbar_init(bar(RFULL), ks > 1 ? (ks - 1) * red_warps * 32 : 1);   // every peer lane
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -360,12 +376,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();   // peer barriers initialised before any remote signal
+    if (clustered) cluster_sync();   // peer barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int kb_per_group = p.k_blocks;
     const int kb_total = p.fold ? p.G * kb_per_group : kb_per_group;
+    // this CTA's k-blocks of each tile (all of them unless K is split)
+    const int kb_lo = (int)((int64_t)kb_total * krank / ks);
+    const int kb_hi = (int)((int64_t)kb_total * (krank + 1) / ks);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -386,9 +405,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
                 const int am0 = m0 + (int)rank * BM;          // this CTA's A rows
                 const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
-                int gk = p.fold ? 0 : g;                      // shard of this k-block
-                int k0 = 0;                                   // its K offset inside the shard
-                for (int kb = 0; kb < kb_total; ++kb, k0 += BK) {
+                // shard of the first k-block and its K offset inside the shard
+                int gk = p.fold ? kb_lo / kb_per_group : g;
+                int k0 = (p.fold ? kb_lo - (kb_lo / kb_per_group) * kb_per_group : kb_lo) * BK;
+                for (int kb = kb_lo; kb < kb_hi; ++kb, k0 += BK) {
                     if (k0 == k_group) {   // folded K loop: next shard
                         k0 = 0;
                         ++gk;
@@ -490,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < kb_total; ++kb) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!wait_fast(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
@@ -507,7 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         if constexpr (PAIR)
                             tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else
-                            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            tc_mma_f16(d_tmem, ad, bd, idesc, ((kb - kb_lo) | k) != 0 ? 1u : 0u);
                     }
                     // frees stage s in both CTAs once these MMAs have read it
                     if constexpr (PAIR)
@@ -543,6 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const uint32_t tempty0 = PAIR ? mapa_shared(bar(TEMPTY), 0) : bar(TEMPTY);
         int acc = 0;
         uint32_t aph = 0;
+        uint32_t rph = 0;   // K split: phase of the exchange barriers
         for (int t = first_tile; t < p.num_tiles; t += tile_step) {
             int g, m0, n0;
             decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
@@ -555,7 +576,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const int row = m0 + (int)rank * BM + quarter * 32 + lane;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            if (!p.dual) {
+            if (ks > 1) {
+                // K split. The leader's stage memory is free once its own MMAs
+                // are done (TFULL); it tells the peers, each peer stores its
+                // partial rows there (slot krank - 1, column groups of 4 x 64
+                // rows, 16 bytes per lane and store) and every storing lane
+                // arrives on the leader's RFULL with release; the leader's
+                // lanes acquire RFULL, add the slots to their own accumulator
+                // and run the epilogue.
+                const bool xfer = quarter < red_warps;           // warp holds rows < 64
+                const uint32_t rrow = (uint32_t)(quarter * 32 + lane);
+                const bool has_k = kb_hi > kb_lo;
+                if (krank == 0) {
+                    if (warp == 2 && lane == 0)
+                        for (int j = 1; j < ks; ++j) mbar_arrive_cluster(mapa_shared(bar(RFREE), (uint32_t)j));
+                    int okr = 1;
+                    if (xfer) okr = wait_acquire_cluster(bar(RFULL), rph, abort_flag, p.err, p.timeout_ns);
+                    if (!__all_sync(0xffffffffu, okr)) break;
+                    for (int c = 0; c < BN; c += 32) {
+                        if (n0 + c >= p.N) break;
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32cols(tbase + (uint32_t)c, r);
+                        tmem_ld_wait();
+                        if (!has_k) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = 0u;
+                        }
+                        if (xfer) {
+                            for (int j = 0; j < ks - 1; ++j) {
+                                const uint32_t slot = sA0 + (uint32_t)(j * C::RED_SLOT_BYTES);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 v = ld_shared_v4(
+                                        slot + ((uint32_t)(c / 4 + q) * KSPLIT_ROWS + rrow) * 16u);
+                                    r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) + v.x);
+                                    r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + v.y);
+                                    r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + v.z);
+                                    r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v.w);
+                                }
+                            }
+                        }
+                        epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                    }
+                } else if (xfer) {
+                    int okf = 1;
+                    if (lane == 0) okf = wait_fast(bar(RFREE), rph, abort_flag, p.err, p.timeout_ns, true);
+                    if (!__shfl_sync(0xffffffffu, okf, 0)) break;
+                    const uint32_t dst0 =
+                        mapa_shared(sA0 + (krank - 1u) * (uint32_t)C::RED_SLOT_BYTES, 0u);
+                    for (int c = 0; c < BN; c += 32) {
+                        if (n0 + c >= p.N) break;
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32cols(tbase + (uint32_t)c, r);
+                        tmem_ld_wait();
+                        if (!has_k) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = 0u;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_cluster_v4(dst0 + ((uint32_t)(c / 4 + q) * KSPLIT_ROWS + rrow) * 16u,
+                                          __uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                          __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    }
+                    mbar_arrive_cluster(mapa_shared(bar(RFULL), 0u));   // release: this lane's stores
+                }
+                rph ^= 1u;
+            } else if (!p.dual) {
                 for (int c = 0; c < BN; c += 32) {
                     if (n0 + c >= p.N) break;
                     uint32_t r[32];
@@ -594,7 +683,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();   // the pair's MMAs and loads are done before TMEM is freed
+    if (clustered) cluster_sync();   // the cluster's MMAs, loads and exchanges are done
     tc_fence_after();
     if (warp == 1) {
         if constexpr (PAIR)
@@ -657,8 +746,46 @@ bool make_map_mn_chunks(CUtensorMap* m, const void* base, int64_t mn, int64_t k,
     return r == CUDA_SUCCESS;
 }
 
+// Co-resident CTAs (cl = 1) or clusters of cl CTAs of one kernel instance on
+// the current device; 0 when the queries fail. Cached per device and cl.
 template <int BN, bool PAIR>
-tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
+int resident_units(int cl) {
+    using C = Cfg<BN, PAIR>;
+    static int units[64][9] = {};
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cl < 1 || cl > 8) return 0;
+    if (units[dev][cl] > 0) return units[dev][cl];
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES) != cudaSuccess)
+            return 0;
+        attr_set[dev] = true;
+    }
+    int n = device_sm_count();
+    if (cl > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.gridDim = dim3((unsigned)(cl * (n / cl)));
+        n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, PAIR>, &cfg) != cudaSuccess) return 0;
+    }
+    units[dev][cl] = n > 0 ? n : 0;
+    return units[dev][cl];
+}
+
+// ks > 1: split each tile's K range across a cluster of ks CTAs (single-CTA
+// tiles, M <= KSPLIT_ROWS, no dual B; one tile per cluster).
+template <int BN, bool PAIR>
+tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     using C = Cfg<BN, PAIR>;
     static TcParams kp;   // large; filled per call under the lock below
     static std::mutex mu;
@@ -717,50 +844,34 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
         kp.raster = shared_a ? 1 : (shared_b ? 2 : 0);
         kp.band = GROUP_M;
     }
+    kp.ksplit = ks;
+    if (ks > 1 && (PAIR || pr.dual || pr.M > KSPLIT_ROWS || ks > C::MAX_KSPLIT || ks > 8 ||
+                   ks > (pr.fold ? G : 1) * kp.k_blocks))
+        return TPMLP_ERR_SHAPE;
     kp.epi = pr.epi;
     kp.err = device_error_word();
     kp.timeout_ns = wait_timeout_ns();
     if (kp.err == nullptr) return TPMLP_ERR_CUDA;
 
-    static bool attr_set[64] = {};
-    static int max_units[64] = {};    // co-resident CTAs (1-CTA) or clusters (pair)
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
-
+    const int cl = PAIR ? 2 : ks;   // CTAs per cluster
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
-    if (PAIR) {
+    if (cl > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = (unsigned)cl;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES) != cudaSuccess)
-            return TPMLP_ERR_CUDA;
-        int units = device_sm_count();
-        if (PAIR) {
-            cfg.gridDim = dim3(2 * (units / 2));
-            int nclusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&nclusters, tc_gemm_kernel<BN, PAIR>, &cfg) !=
-                    cudaSuccess ||
-                nclusters < 1)
-                return TPMLP_ERR_CUDA;
-            units = nclusters;
-        }
-        max_units[dev] = units;
-        attr_set[dev] = true;
-    }
-    const int units = kp.num_tiles < max_units[dev] ? kp.num_tiles : max_units[dev];
-    cfg.gridDim = dim3(units * C::CTAS);
+    const int max_units = resident_units<BN, PAIR>(PAIR ? 2 : 1);
+    if (max_units < 1) return TPMLP_ERR_CUDA;
+    // persistent units, or one cluster per tile when K is split
+    const int units = ks > 1 ? kp.num_tiles : (kp.num_tiles < max_units ? kp.num_tiles : max_units);
+    cfg.gridDim = dim3((unsigned)(units * cl));
     cudaError_t e;
     {
         LaunchScope ls(pr.name, s);
@@ -772,43 +883,94 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s) {
 
 }  // namespace
 
-tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
-    if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
-    if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
+namespace {
+
+struct Plan {
+    int bn;
+    bool pair;
+    int ks;
+    bool ok;
+};
+
+Plan choose_plan(const GemmProblem& pr) {
     // Tile choice by estimated time = waves x per-tile cost. A wave is one
-    // tile per CTA (single) or per CTA pair; the per-tile cost is its MMA work
-    // over the relative rate measured for the tile shape, or, for a few rows
-    // (M <= 64: weight streaming, HBM-bound), the operand bytes it streams,
-    // which grow with BN.
+    // tile per CTA (single), per CTA pair, or per K-split cluster; the
+    // per-tile cost is its MMA work over the relative rate measured for the
+    // tile shape, or, for a few rows (M <= 64: weight streaming, HBM-bound),
+    // the operand bytes each CTA streams plus a fixed start cost.
+    // K-split candidates (M <= 64, weight streaming): a cluster of ks CTAs
+    // shares one tile's K range, so each streams 1/ks of the tile's bytes and
+    // more SMs stream when the tiles are fewer than the SMs.
     struct Cand {
         int bn;
         bool pair;
+        int ks;
         double rate;
     };
-    const Cand cands[3] = {{256, true, 1.08}, {256, false, 1.0}, {128, false, 0.85}};
-    const int sms = device_sm_count();
+    const Cand cands[] = {{256, true, 1, 1.08}, {256, false, 1, 1.0}, {128, false, 1, 0.85},
+                          {256, false, 2, 1.0},  {256, false, 3, 1.0}, {256, false, 4, 1.0},
+                          {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85}};
+    const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
     const int groups = pr.fold ? 1 : pr.G;
+    const int64_t kb_total = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + 63) / 64);
     double best = 1e300;
     int pick = 1;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < ncand; ++i) {
         const Cand& c = cands[i];
         if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
+        if (c.ks > 1 && (pr.M > KSPLIT_ROWS || pr.dual || c.ks > kb_total)) continue;
         const int64_t tile_m = c.pair ? 256 : 128;
         const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
         const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
                               ((pr.N + n_out - 1) / n_out);
-        const int64_t units = c.pair ? sms / 2 : sms;
+        int64_t units = 0;
+        if (c.bn == 128) units = resident_units<128, false>(c.ks);
+        else if (c.pair) units = resident_units<256, true>(2);
+        else units = resident_units<256, false>(c.ks);
+        if (units < 1) continue;
         const int64_t waves = (tiles + units - 1) / units;
-        const double cost = pr.M <= 64 ? (double)waves * c.bn
-                                        : (double)waves * 128.0 * c.bn / c.rate;
+        // M <= 64: streamed bytes in units of (tile columns x k-blocks), plus a
+        // fixed cost per CTA start (launch, TMEM, barrier set-up, pipeline
+        // fill, the K-split exchange) of about 30 k-blocks of a 128-column
+        // tile, fitted on the N = 16, D = 12288, F = 49152 forward; a
+        // persistent launch pays it once, a K-split launch once per wave
+        const double start = 30.0 * 128.0;
+        const double kb_cta = (double)((kb_total + c.ks - 1) / c.ks);
+        double cost;
+        if (pr.M > 64)
+            cost = (double)waves * 128.0 * c.bn / c.rate;
+        else if (c.ks == 1)
+            cost = start + (double)waves * c.bn * kb_cta;
+        else
+            cost = (double)waves * (start + c.bn * kb_cta);
         if (cost < best) {
             best = cost;
             pick = i;
         }
     }
-    if (cands[pick].bn == 128) return launch<128, false>(pr, s);
-    if (cands[pick].pair) return launch<256, true>(pr, s);
-    return launch<256, false>(pr, s);
+    return Plan{cands[pick].bn, cands[pick].pair, cands[pick].ks, best < 1e299};
+}
+
+}  // namespace
+
+tpmlp_status plan_gemm_tc(const GemmProblem& pr, int* bn, int* mma_ctas, int* ksplit) {
+    if (pr.M <= 0 || pr.N <= 0 || pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
+    const Plan c = choose_plan(pr);
+    if (!c.ok) return TPMLP_ERR_CUDA;
+    *bn = c.bn;
+    *mma_ctas = c.pair ? 2 : 1;
+    *ksplit = c.ks;
+    return TPMLP_OK;
+}
+
+tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
+    if (pr.M <= 0 || pr.N <= 0) return TPMLP_OK;
+    if (pr.K <= 0 || pr.G < 1 || pr.G > kMaxG) return TPMLP_ERR_SHAPE;
+    const Plan c = choose_plan(pr);
+    if (!c.ok) return TPMLP_ERR_CUDA;
+    if (c.bn == 128) return launch<128, false>(pr, s, c.ks);
+    if (c.pair) return launch<256, true>(pr, s);
+    return launch<256, false>(pr, s, c.ks);
 }
 
 }  // namespace tpmlp

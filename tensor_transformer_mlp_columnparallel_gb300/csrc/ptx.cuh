@@ -84,6 +84,47 @@ __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatil
     return wait_bounded(bar, parity, abort_flag, err, timeout_ns, watch_abort);
 }
 
+// As wait_bounded, then a try_wait with acquire at cluster scope, for a phase
+// completed by release arrives from other CTAs of the cluster that publish
+// their shared-memory stores. Off the hot loops: a cluster-scope acquire is
+// costly when polled.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_acquire_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     int* err, uint64_t timeout_ns) {
+    // once complete the phase stays complete until this CTA consumes it again,
+    // so the cluster-scope try_wait after the bounded wait succeeds at once
+    return wait_bounded(bar, parity, abort_flag, err, timeout_ns, true) &&
+           mbar_try_wait_cluster(bar, parity);
+}
+
+// 16-byte store into another CTA's shared memory (a shared::cluster address
+// from mapa_shared) and 16-byte load from this CTA's shared memory.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---- clusters -------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

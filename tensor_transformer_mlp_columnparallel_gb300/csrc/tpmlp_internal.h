@@ -61,6 +61,9 @@ struct GemmProblem {
 
 // bf16 inputs on tcgen05 tensor cores (TMA + mbarrier pipeline + TMEM).
 tpmlp_status run_gemm_tc(const GemmProblem& p, cudaStream_t s);
+// The tile configuration run_gemm_tc launches for p (accumulator columns,
+// CTAs per MMA, K-split cluster size); nothing is launched.
+tpmlp_status plan_gemm_tc(const GemmProblem& p, int* bn, int* mma_ctas, int* ksplit);
 // fp32 inputs on CUDA cores (exact fp32 FMA, no TF32).
 tpmlp_status run_gemm_simt(const GemmProblem& p, cudaStream_t s);
 

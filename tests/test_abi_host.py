@@ -128,6 +128,16 @@ def test_vocab_ce_and_reduce_errors(lib):
     assert lib.tpmlp_block_reduce(3, 4, 8, 2, ptrs(FAKE, FAKE), None, FAKE, None) == B.ERR_DTYPE
 
 
+def test_gemm_plan_argument_errors(lib):
+    x = ctypes.c_int(0)
+    r = ctypes.byref(x)
+    assert lib.tpmlp_gemm_plan(16, 128, 64, 1, 0, 0, None, r, r) == B.ERR_ARG
+    assert lib.tpmlp_gemm_plan(0, 128, 64, 1, 0, 0, r, r, r) == B.ERR_SHAPE
+    assert lib.tpmlp_gemm_plan(16, 128, 64, 0, 0, 0, r, r, r) == B.ERR_SHAPE
+    assert lib.tpmlp_gemm_plan(16, 128, 64, 17, 1, 0, r, r, r) == B.ERR_SHAPE
+    assert lib.tpmlp_gemm_plan(1 << 31, 128, 64, 1, 0, 0, r, r, r) == B.ERR_SHAPE
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
