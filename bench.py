@@ -380,7 +380,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     del parts, rows_out
     torch.cuda.empty_cache()
     # vocab-parallel embedding: table 32000 x 8192 bf16 over T = 4 (the textbook
-    # page's row-parallel embedding), 8192 tokens; L2 flushed before every launch
+    # page's row-parallel embedding), 8192 tokens; L2 flushed (by a read) before every launch
     Ve, He, Te, Ne = 32000, 8192, 4, 8192
     ge = torch.Generator(device=dev)
     ge.manual_seed(0)
@@ -388,10 +388,13 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
               for _ in range(Te)]
     ids = torch.randint(0, Ve, (Ne,), generator=ge, device=dev)
     emb = torch.empty(Ne, He, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush by READING a buffer twice the L2 size: L2 then holds clean lines,
+    # so no write-back of flush data (or of the previous output, which the
+    # flush evicts) lands inside the timed launch
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     tp.tpmlp_timing_reset()
     for i in range(3 + steps):
-        flush.fill_(i & 0xff)
+        flush.max()
         if i == 3:
             tp.tpmlp_timing_enable(True)
         tp.tpmlp_vocab_embedding(ids, shards, emb)
@@ -402,7 +405,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     e_bytes = 2.0 * Ne * He * 2 + Ne * 8
     gbs = e_bytes / (ms * 1e-3) / 1e9
     out["vocab_embedding_v32000_h8192_t4_n8192"] = {
-        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs, "l2": "flushed before each launch",
+        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs, "l2": "flushed before each launch by reading a 256 MB buffer",
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": e_bytes,
                      "traffic": load_traffic("vocab_embedding")}}

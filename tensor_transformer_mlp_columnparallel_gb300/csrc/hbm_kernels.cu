@@ -473,6 +473,84 @@ __global__ void __launch_bounds__(256) vocab_embedding_kernel(const EmbParams p)
     }
 }
 
+// Bulk-copy form (16-byte aligned rows whose size is a multiple of 16 bytes):
+// one thread per CTA streams row chunks global -> shared -> global with
+// cp.async.bulk, EMB_BUFS chunks deep, so each SM keeps several 16 KB chunks
+// in flight with almost no instructions issued. An id outside [0, V) gives a
+// zero row (written with plain stores) and TPMLP_ERR_ARG.
+constexpr int EMB_BUFS = 4;
+constexpr int EMB_CHUNK = 16384;
+constexpr int EMB_SMEM = EMB_BUFS * EMB_CHUNK;
+
+__global__ void __launch_bounds__(32) vocab_embedding_bulk_kernel(const EmbParams p, uint64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t ebuf[];
+    __shared__ __align__(8) uint64_t bars[EMB_BUFS];
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    for (int b = 0; b < EMB_BUFS; ++b) mbar_init(smem_u32(&bars[b]), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    const int64_t cpr = (p.row_bytes + EMB_CHUNK - 1) / EMB_CHUNK;   // chunks per row
+    const int64_t items = p.N * cpr;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t count = items > first ? (items - 1 - first) / step + 1 : 0;
+    // item j of this CTA: token n, chunk c; returns false for an invalid id
+    auto locate = [&](int64_t j, const char*& src, char*& dst, uint32_t& bytes) -> bool {
+        const int64_t it = first + j * step;
+        const int64_t n = it / cpr, c = it - n * cpr;
+        const int64_t off = c * EMB_CHUNK;
+        const int64_t rem = p.row_bytes - off;
+        bytes = (uint32_t)(rem < EMB_CHUNK ? rem : EMB_CHUNK);
+        dst = static_cast<char*>(p.out) + n * p.row_bytes + off;
+        const int64_t id = p.ids[n];
+        if (id < 0 || id >= p.V) {
+            src = nullptr;
+            return false;
+        }
+        const int64_t k = id / p.Vs;
+        src = static_cast<const char*>(p.table[k]) + (id - k * p.Vs) * p.row_bytes + off;
+        return true;
+    };
+    auto issue = [&](int64_t j) {
+        const uint32_t bar = smem_u32(&bars[j % EMB_BUFS]);
+        const char* src;
+        char* dst;
+        uint32_t bytes;
+        if (locate(j, src, dst, bytes)) {
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load_g2s(smem_u32(ebuf) + (uint32_t)(j % EMB_BUFS) * EMB_CHUNK, src, bytes, bar);
+        } else {
+            mbar_arrive(bar);   // keeps the buffer's phase count in step
+        }
+    };
+    int64_t issued = 0;
+    for (; issued < count && issued < EMB_BUFS; ++issued) issue(issued);
+    int64_t i = 0;
+    for (; i < count; ++i) {
+        const int b = (int)(i % EMB_BUFS);
+        const uint32_t parity = (uint32_t)((i / EMB_BUFS) & 1);
+        if (!wait_bounded(smem_u32(&bars[b]), parity, &abort_flag, p.err, timeout_ns, false)) break;
+        const char* src;
+        char* dst;
+        uint32_t bytes;
+        if (locate(i, src, dst, bytes)) {
+            bulk_store_s2g(dst, smem_u32(ebuf) + (uint32_t)b * EMB_CHUNK, bytes);
+            bulk_commit();
+            bulk_wait_read_all();   // buffer b may be refilled once its store has read it
+        } else {
+            atomicCAS(p.err, 0, (int)TPMLP_ERR_ARG);
+            for (uint32_t q = 0; q < bytes; q += 16)
+                *reinterpret_cast<uint4*>(dst + q) = make_uint4(0, 0, 0, 0);
+        }
+        if (issued < count) issue(issued++);
+    }
+    // after a timeout: wait (bounded) for the loads still in flight
+    for (; i < issued; ++i)
+        wait_bounded(smem_u32(&bars[i % EMB_BUFS]), (uint32_t)((i / EMB_BUFS) & 1), &abort_flag, p.err,
+                     timeout_ns, false);
+    bulk_wait_all();
+}
+
 // ------------------------------------------------------------- self test --
 
 __global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
@@ -623,10 +701,26 @@ tpmlp_status run_vocab_embedding(int f32, int64_t N, int64_t V, int64_t H, int T
     kp.vec = vec;
     kp.err = device_error_word();
     if (kp.err == nullptr) return TPMLP_ERR_CUDA;
-    const int64_t max_grid = (int64_t)device_sm_count() * 8;
-    int64_t grid = (N + 7) / 8;            // 8 warps per CTA, one token each
-    if (grid > max_grid) grid = max_grid;
-    {
+    if (vec) {
+        // bulk copies: three 64 KB CTAs per SM
+        static bool attr_set[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(vocab_embedding_bulk_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, EMB_SMEM) != cudaSuccess)
+                return TPMLP_ERR_CUDA;
+            attr_set[dev] = true;
+        }
+        const int64_t items = N * ((kp.row_bytes + EMB_CHUNK - 1) / EMB_CHUNK);
+        const int64_t max_grid = (int64_t)device_sm_count() * 3;
+        const int64_t grid = items < max_grid ? items : max_grid;
+        LaunchScope ls("vocab_embedding", s);
+        vocab_embedding_bulk_kernel<<<(unsigned)grid, 32, EMB_SMEM, s>>>(kp, wait_timeout_ns());
+    } else {
+        const int64_t max_grid = (int64_t)device_sm_count() * 8;
+        int64_t grid = (N + 7) / 8;            // 8 warps per CTA, one token each
+        if (grid > max_grid) grid = max_grid;
         LaunchScope ls("vocab_embedding", s);
         vocab_embedding_kernel<<<(unsigned)grid, 256, 0, s>>>(kp);
     }

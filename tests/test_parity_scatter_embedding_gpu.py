@@ -115,3 +115,23 @@ def test_vocab_embedding_odd_width_and_bad_ids():
     assert tp.tpmlp_check_device_error() == _binding.ERR_ARG
     np.testing.assert_array_equal(f64(out), oracle.embedding.vocab_embedding(ids, E))
     np.testing.assert_array_equal(f64(out), oracle.sharded.vocab_embedding_sharded(ids, E, T))
+
+
+@pytest.mark.parametrize("Hd", [8, 8192, 8200, 20480])
+def test_vocab_embedding_bulk_path_rows_chunks_and_bad_ids(Hd):
+    """16-byte aligned rows take the bulk-copy path: rows of one chunk, of
+    exactly one 16 KB chunk, of a chunk plus a 16-byte tail, and of several
+    chunks; bad ids (outside [0, V)) give zero rows and TPMLP_ERR_ARG."""
+    V, T = 40, 4
+    g = torch.Generator().manual_seed(Hd)
+    E = torch.randn(V, Hd, generator=g).to(torch.bfloat16)
+    ids = torch.randint(0, V, (300,), generator=g)
+    ids[7], ids[150], ids[299] = -1, V, 10 * V
+    shards = [E[k * (V // T):(k + 1) * (V // T)].contiguous().to(dev()) for k in range(T)]
+    out = tp.vocab_embedding(ids.to(dev()), shards)
+    assert tp.tpmlp_check_device_error() == _binding.ERR_ARG
+    np.testing.assert_array_equal(f64(out), oracle.embedding.vocab_embedding(ids, E))
+    good = ids[(ids >= 0) & (ids < V)][:64]
+    out2 = tp.vocab_embedding(good.to(dev()), shards)
+    assert tp.tpmlp_check_device_error() == 0
+    np.testing.assert_array_equal(f64(out2), oracle.embedding.vocab_embedding(good, E))
