@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="N,D,F,T override of the fwd+bwd workload (small cases for profiling)")
+    ap.add_argument("--only-embedding", action="store_true",
+                    help="time only the vocab embedding gather (32000 x 8192 bf16, T=4, 8192 ids)")
     ap.add_argument("--only-ce", type=int, default=0, metavar="TOKENS",
                     help="time only the vocab CE forward and backward (V=128000, T=8) on TOKENS "
                          "tokens (small cases for profiling)")
@@ -307,6 +309,42 @@ def cpu_baseline_mlp(cfg, tokens=96):
                       f"host cores), {dt:.1f} s"}
 
 
+def measure_embedding(dev, steps, pk):
+    """Vocab-parallel embedding: table 32000 x 8192 bf16 over T = 4 (the
+    textbook page's row-parallel embedding), 8192 tokens; L2 flushed by a read
+    before every launch. Returns the record of the secondary measurements."""
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+    Ve, He, Te, Ne = 32000, 8192, 4, 8192
+    ge = torch.Generator(device=dev)
+    ge.manual_seed(0)
+    shards = [(torch.randn(Ve // Te, He, generator=ge, device=dev) * 0.02).to(torch.bfloat16)
+              for _ in range(Te)]
+    ids = torch.randint(0, Ve, (Ne,), generator=ge, device=dev)
+    emb = torch.empty(Ne, He, dtype=torch.bfloat16, device=dev)
+    # L2 flush by READING a buffer twice the L2 size: L2 then holds clean lines,
+    # so no write-back of flush data (or of the previous output, which the
+    # flush evicts) lands inside the timed launch
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    tp.tpmlp_timing_reset()
+    for i in range(3 + steps):
+        flush.max()
+        if i == 3:
+            tp.tpmlp_timing_enable(True)
+        tp.tpmlp_vocab_embedding(ids, shards, emb)
+    torch.cuda.synchronize()
+    tp.tpmlp_timing_enable(False)
+    k = tp.tpmlp_timing_read()["vocab_embedding"]
+    ms = k["total_ms"] / k["launches"]
+    e_bytes = 2.0 * Ne * He * 2 + Ne * 8
+    gbs = e_bytes / (ms * 1e-3) / 1e9
+    return {
+        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs,
+        "l2": "flushed before each launch by reading a 256 MB buffer",
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": e_bytes,
+                     "traffic": load_traffic("vocab_embedding")}}
+
+
 def secondary(dev, stream, steps, pk, ce_tokens=0):
     import dataclasses
     import tensor_transformer_mlp_columnparallel_gb300 as tp
@@ -379,37 +417,7 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
                      "traffic": load_traffic("block_reduce_scatter_bias")}}
     del parts, rows_out
     torch.cuda.empty_cache()
-    # vocab-parallel embedding: table 32000 x 8192 bf16 over T = 4 (the textbook
-    # page's row-parallel embedding), 8192 tokens; L2 flushed (by a read) before every launch
-    Ve, He, Te, Ne = 32000, 8192, 4, 8192
-    ge = torch.Generator(device=dev)
-    ge.manual_seed(0)
-    shards = [(torch.randn(Ve // Te, He, generator=ge, device=dev) * 0.02).to(torch.bfloat16)
-              for _ in range(Te)]
-    ids = torch.randint(0, Ve, (Ne,), generator=ge, device=dev)
-    emb = torch.empty(Ne, He, dtype=torch.bfloat16, device=dev)
-    # L2 flush by READING a buffer twice the L2 size: L2 then holds clean lines,
-    # so no write-back of flush data (or of the previous output, which the
-    # flush evicts) lands inside the timed launch
-    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
-    tp.tpmlp_timing_reset()
-    for i in range(3 + steps):
-        flush.max()
-        if i == 3:
-            tp.tpmlp_timing_enable(True)
-        tp.tpmlp_vocab_embedding(ids, shards, emb)
-    torch.cuda.synchronize()
-    tp.tpmlp_timing_enable(False)
-    k = tp.tpmlp_timing_read()["vocab_embedding"]
-    ms = k["total_ms"] / k["launches"]
-    e_bytes = 2.0 * Ne * He * 2 + Ne * 8
-    gbs = e_bytes / (ms * 1e-3) / 1e9
-    out["vocab_embedding_v32000_h8192_t4_n8192"] = {
-        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs, "l2": "flushed before each launch by reading a 256 MB buffer",
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": e_bytes,
-                     "traffic": load_traffic("vocab_embedding")}}
-    del shards, emb, flush
+    out["vocab_embedding_v32000_h8192_t4_n8192"] = measure_embedding(dev, steps, pk)
     torch.cuda.empty_cache()
     # forward-only workloads: N=4096 D=4096 F=16384 T=4 (tensor-bound) and
     # N=16 D=12288 F=49152 T=8 (weight streaming, HBM-bound)
@@ -709,10 +717,22 @@ def run_only_ce(args):
     print(json.dumps({"only": "vocab_ce", "tokens": args.only_ce, "results": out}))
 
 
+def run_only_embedding(args):
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    print(json.dumps({"only": "vocab_embedding",
+                      "results": measure_embedding(dev, args.steps, peaks())}))
+
+
 def main():
     args = parse()
     if args.only_ce:
         run_only_ce(args)
+        return
+    if args.only_embedding:
+        run_only_embedding(args)
         return
     if args.impl == "reference":
         run_reference(args)
