@@ -267,9 +267,9 @@ tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * all G groups into one output (the split-K shard sum), dual = 1 for the
  * gated GEMM (N counts outputs). Writes the tile's accumulator columns (128
  * or 256), the CTAs that issue one MMA (1, or 2 for a CTA pair) and the CTAs
- * of a cluster that share one tile's K range (1 = no split; used for
- * M <= 64, where the weights stream from HBM and the tiles are fewer than
- * the SMs). A query: launches nothing. Returns TPMLP_ERR_ARG for a null
+ * of a cluster that share one tile's K range (1 = no split; used for folded
+ * GEMMs with M <= 64, where the weights stream from HBM and the tiles are
+ * fewer than the SMs). A query: launches nothing. Returns TPMLP_ERR_ARG for a null
  * output pointer, TPMLP_ERR_SHAPE for sizes < 1 or above 2^31 - 1 or G
  * outside [1, TPMLP_MAX_SHARDS], TPMLP_ERR_CUDA when the device queries fail.
  * Library introspection; the source pages have no counterpart. */

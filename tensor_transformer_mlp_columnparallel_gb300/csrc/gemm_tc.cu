@@ -898,9 +898,9 @@ Plan choose_plan(const GemmProblem& pr) {
     // per-tile cost is its MMA work over the relative rate measured for the
     // tile shape, or, for a few rows (M <= 64: weight streaming, HBM-bound),
     // the operand bytes each CTA streams plus a fixed start cost.
-    // K-split candidates (M <= 64, weight streaming): a cluster of ks CTAs
-    // shares one tile's K range, so each streams 1/ks of the tile's bytes and
-    // more SMs stream when the tiles are fewer than the SMs.
+    // K-split candidates (folded GEMMs, M <= 64, weight streaming): a cluster
+    // of ks CTAs shares one tile's K range, so each streams 1/ks of the tile's
+    // bytes and more SMs stream when the tiles are fewer than the SMs.
     struct Cand {
         int bn;
         bool pair;
@@ -918,7 +918,10 @@ Plan choose_plan(const GemmProblem& pr) {
     for (int i = 0; i < ncand; ++i) {
         const Cand& c = cands[i];
         if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
-        if (c.ks > 1 && (pr.M > KSPLIT_ROWS || pr.dual || c.ks > kb_total)) continue;
+        // K split only for the folded GEMMs (the split-K shard sum): folding
+        // leaves N / BN tiles, where a grouped GEMM has T times as many; on the
+        // grouped ones a split measured slower or equal on every decode shape
+        if (c.ks > 1 && (!pr.fold || pr.M > KSPLIT_ROWS || pr.dual || c.ks > kb_total)) continue;
         const int64_t tile_m = c.pair ? 256 : 128;
         const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
         const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
