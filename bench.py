@@ -263,13 +263,18 @@ def kernel_family(kernel):
 
 
 def kernel_source_hash(family="gemm"):
-    """sha256 over the CUDA sources of one kernel family (file name + bytes)."""
+    """sha256 over the CUDA sources of one kernel family: file names and the
+    code with `//` comments, trailing blanks and empty lines removed, so that
+    editing a comment does not invalidate a capture of the same code."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "tensor_transformer_mlp_columnparallel_gb300", "csrc")
     for f in KERNEL_FAMILIES[family]:
         h.update(f.encode())
-        h.update(open(os.path.join(d, f), "rb").read())
+        for line in open(os.path.join(d, f), encoding="utf-8"):
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 
