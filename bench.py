@@ -457,6 +457,24 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
             out[f"{name}_{mode}"] = rec
         del fb
         torch.cuda.empty_cache()
+    # the exact-fp32 block, N=64 D=256 F=1024 T=2 (ReLU, biases): latency-bound
+    # (67 MFLOP forward), so time per call, eager and replayed from a CUDA graph
+    fc = MLP_CONFIGS["mlp_f32_relu_n64_d256_f1024_t2"]
+    fb = Block(fc, "splitk", dev)
+    rec = {"note": "latency-bound; time reported, no roofline claim"}
+    for label, fn in (("forward", fb.forward), ("forward+backward", fb.step)):
+        ms_e = timed(fn, steps, 3, 1, dev, stream) / steps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(10):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        ms_g = timed(graph.replay, max(1, steps // 10), 1, 1, dev, stream) / (10 * max(1, steps // 10))
+        rec[label] = {"us_per_call_eager": ms_e * 1e3, "us_per_call_graph": ms_g * 1e3}
+    out["mlp_f32_relu_n64_d256_f1024_t2_latency"] = rec
+    del fb
+    torch.cuda.empty_cache()
     # gated (SwiGLU) block, N=4096 D=4096 F=16384 T=4: gate and up as one dual
     # GEMM per shard, then the split-K down projection
     Ns, Ds, Fg, Tg = 4096, 4096, 16384, 4

@@ -1,7 +1,8 @@
 // fp32 grouped / shard-folded GEMM on CUDA cores: the exact-fp32 mode of the
 // block (fmaf in fp32, no TF32 tensor cores, whose 10-bit mantissa would not
 // meet a 1e-5 relative bound). 64 x 64 output tile per CTA, 256 threads,
-// 4 x 4 outputs per thread, K staged through shared memory 16 at a time.
+// 4 x 4 outputs per thread, K staged through shared memory 16 at a time with
+// the next chunk's loads in flight in registers.
 // Same problem description and epilogue semantics as the tensor-core GEMM.
 #include "act.cuh"
 #include "tpmlp_internal.h"
@@ -57,59 +58,79 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = acc2[i][j] = 0.f;
 
+    // The K loop (over (shard, k) when folded) walks chunks of TK; the global
+    // loads of chunk c + 1 go to registers while chunk c is computed from
+    // shared memory, so a CTA waits for memory once, not once per chunk.
     const int ngroups = p.fold ? p.G : 1;
-    for (int gi = 0; gi < ngroups; ++gi) {
+    const int kchunks = (p.K + TK - 1) / TK;
+    const int nchunks = ngroups * kchunks;
+    constexpr int PER = TM * TK / 256;   // A (and B) elements each thread stages
+    static_assert(TM * TK == 256 * PER && TN * TK == 256 * PER, "staging split");
+    float ra[PER], rb[PER], rb2[PER];
+    auto fetch = [&](int c) {
+        const int gi = c / kchunks;
+        const int k0 = (c - gi * kchunks) * TK;
         const int g = p.fold ? gi : (int)blockIdx.z;
         const float* A = p.A[g];
         const float* B = p.B[g];
         const float* B2 = p.B2[g];
-        for (int k0 = 0; k0 < p.K; k0 += TK) {
-            for (int i = threadIdx.x; i < TM * TK; i += 256) {
-                const int mm = A_MN ? i % TM : i / TK;
-                const int kk = A_MN ? i / TM : i % TK;
-                const int m = m0 + mm, k = k0 + kk;
-                float v = 0.f;
-                if (m < p.M && k < p.K)
-                    v = A_MN ? A[(int64_t)k * p.lda + m] : A[(int64_t)m * p.lda + k];
-                As[kk][mm] = v;
-            }
-            for (int i = threadIdx.x; i < TN * TK; i += 256) {
-                const int nn = B_MN ? i % TN : i / TK;
-                const int kk = B_MN ? i / TN : i % TK;
-                const int n = n0 + nn, k = k0 + kk;
-                float v = 0.f;
-                if (n < p.N && k < p.K)
-                    v = B_MN ? B[(int64_t)k * p.ldb + n] : B[(int64_t)n * p.ldb + k];
-                Bs[kk][nn] = v;
-                if (DUAL) {
-                    float v2 = 0.f;
-                    if (n < p.N && k < p.K)
-                        v2 = B_MN ? B2[(int64_t)k * p.ldb + n] : B2[(int64_t)n * p.ldb + k];
-                    Bs2[kk][nn] = v2;
-                }
-            }
-            __syncthreads();
 #pragma unroll
-            for (int kk = 0; kk < TK; ++kk) {
-                float a[4], b[4];
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            const int mm = A_MN ? i % TM : i / TK;
+            const int ka = A_MN ? i / TM : i % TK;
+            const int m = m0 + mm, k = k0 + ka;
+            ra[u] = (m < p.M && k < p.K) ? (A_MN ? A[(int64_t)k * p.lda + m] : A[(int64_t)m * p.lda + k])
+                                         : 0.f;
+            const int nn = B_MN ? i % TN : i / TK;
+            const int kb = B_MN ? i / TN : i % TK;
+            const int n = n0 + nn, kq = k0 + kb;
+            const bool in = n < p.N && kq < p.K;
+            rb[u] = in ? (B_MN ? B[(int64_t)kq * p.ldb + n] : B[(int64_t)n * p.ldb + kq]) : 0.f;
+            if (DUAL)
+                rb2[u] = in ? (B_MN ? B2[(int64_t)kq * p.ldb + n] : B2[(int64_t)n * p.ldb + kq]) : 0.f;
+        }
+    };
+    auto stash = [&]() {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + 256 * u;
+            As[A_MN ? i / TM : i % TK][A_MN ? i % TM : i / TK] = ra[u];
+            const int nn = B_MN ? i % TN : i / TK;
+            const int kb = B_MN ? i / TN : i % TK;
+            Bs[kb][nn] = rb[u];
+            if (DUAL) Bs2[kb][nn] = rb2[u];
+        }
+    };
+    fetch(0);
+    stash();
+    __syncthreads();
+    for (int c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks) fetch(c + 1);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+        for (int kk = 0; kk < TK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            if (DUAL) {
+                float b2[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b2[j] = Bs2[kk][tx + 16 * j];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                if (DUAL) {
-                    float b2[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) b2[j] = Bs2[kk][tx + 16 * j];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
-                }
+                    for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
             }
+        }
+        __syncthreads();
+        if (c + 1 < nchunks) {
+            stash();
             __syncthreads();
         }
     }
