@@ -72,7 +72,9 @@ typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
  *   and casts (the single-GPU form of the all-reduce).
  * SPLITK: the row GEMM runs its K loop over (r, k) into one fp32 accumulator,
  *   so the shard sum never leaves the tensor-core accumulator; b2 is added
- *   once in the epilogue. No workspace. */
+ *   once in the epilogue. No workspace. (For N <= 64 tokens the (r, k) loop
+ *   of a tile may be split across a cluster of 2-4 CTAs whose partial
+ *   accumulators are added in on-chip shared memory; see tpmlp_gemm_plan.) */
 typedef enum { TPMLP_REDUCE_PARTIALS = 0, TPMLP_REDUCE_SPLITK = 1 } tpmlp_reduce_mode;
 
 typedef enum { TPMLP_OP_FORWARD = 0, TPMLP_OP_BACKWARD = 1 } tpmlp_op;
