@@ -53,6 +53,28 @@ def test_forward_reduce_scatter_matches_all_reduce_and_oracle(mode, dtype, T):
         assert_close(Y_rows[r], f["Y"][r * Ns:(r + 1) * Ns], dtype, f"rank {r} rows")
 
 
+@pytest.mark.parametrize("N,T", [(32, 2), (64, 4), (16, 8)])
+def test_forward_reduce_scatter_through_the_k_split(N, T):
+    """A few tokens: the split-K row GEMM shares each tile's k-blocks across a
+    CTA cluster, and the leader's epilogue writes rank r's rows into Y_rows[r]
+    after adding the peers' partials (with b2 once)."""
+    D, Fs = 1024, 512
+    assert tp.tpmlp_gemm_plan(N, D, Fs, T, fold=True)[2] > 1
+    inp = gen_random_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", act="gelu_tanh", bias=True,
+                         seed=90 + T, with_dy=False)
+    g = to_gpu(inp)
+    Y_rows, _, _ = tp.mlp_forward_reduce_scatter(g["X"], g["W1"], g["W2"], g["b1"], g["b2"],
+                                                 act="gelu_tanh", mode="splitk")
+    Y, _, _ = tp.mlp_forward(g["X"], g["W1"], g["W2"], g["b1"], g["b2"], act="gelu_tanh",
+                             mode="splitk")
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(Y_rows, 0), Y)
+    f = oracle.mlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh")
+    Ns = N // T
+    for r in range(T):
+        assert_close(Y_rows[r], f["Y"][r * Ns:(r + 1) * Ns], "bf16", f"rank {r} rows")
+
+
 def test_forward_reduce_scatter_integer_inputs_bit_exact():
     T = 4
     inp = gen_integer_mlp(N=128, D=16, F=64, T=T, dtype="bf16", bias=True, seed=8, with_dy=False)
