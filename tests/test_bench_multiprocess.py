@@ -65,3 +65,20 @@ def test_single_process_defaults():
         os.environ.pop(k, None)
     assert bench.dist_env() == (0, 1, 0)
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
+
+
+def test_kernel_source_hash_ignores_comments_but_not_code(monkeypatch, tmp_path):
+    """The committed DRAM traffic is keyed by this hash: editing a comment
+    must keep it, editing code must change it."""
+    import bench
+    csrc = tmp_path / "tensor_transformer_mlp_columnparallel_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    f = csrc / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_FAMILIES", {"gemm": ("k.cu",)})
+    f.write_text("// kernel\nint x = 1;  // one\n\n")
+    h0 = bench.kernel_source_hash("gemm")
+    f.write_text("// the kernel, reworded\n\nint x = 1;    // still one\n")
+    assert bench.kernel_source_hash("gemm") == h0
+    f.write_text("// kernel\nint x = 2;  // one\n")
+    assert bench.kernel_source_hash("gemm") != h0
