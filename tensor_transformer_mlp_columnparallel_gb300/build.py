@@ -52,18 +52,28 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not verbose_ptxas and not _stale():
-        return LIB
+    """Compiles and links libtpmlp.so when a source is newer than it. Several
+    processes may call this at once (one per rank): an exclusive lock on a
+    file in the build folder lets one of them build while the others wait
+    and then find the library fresh."""
+    import fcntl
     os.makedirs(BUILD, exist_ok=True)
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = os.path.join(BUILD, "libtpmlp.partial.so")
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not verbose_ptxas and not _stale():
+                return LIB
+            with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+                objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
+            tmp = os.path.join(BUILD, "libtpmlp.partial.so")
+            cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, LIB)
+            return LIB
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
 
 
 if __name__ == "__main__":
