@@ -147,6 +147,26 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // every committed store has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Bounded wait that sleeps between polls, for a thread with slack (the
+// epilogue waiting for an accumulator): spinning would take issue slots from
+// the TMA and MMA threads on the same sub-partition, whose loops are
+// latency-critical. Same abort / timeout behaviour as wait_bounded.
+static __device__ __noinline__ bool wait_sleepy(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err, uint64_t timeout_ns, uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicCAS(err, 0, 6 /* TPMLP_ERR_TIMEOUT */);
+            return false;
+        }
+    }
+}
+
 // ---- clusters -------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
