@@ -763,6 +763,8 @@ int resident_units(int cl) {
     using C = Cfg<BN, PAIR>;
     static int units[64][9] = {};
     static bool attr_set[64] = {};
+    static std::mutex mu;   // first calls may come from several host threads
+    std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cl < 1 || cl > 8) return 0;
     if (units[dev][cl] > 0) return units[dev][cl];

@@ -15,6 +15,7 @@
 //   LM-head bullets; Megatron TP chapter §7.8). One pass over the logits.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "act.cuh"
@@ -703,14 +704,15 @@ tpmlp_status run_vocab_embedding(int f32, int64_t N, int64_t V, int64_t H, int T
     if (kp.err == nullptr) return TPMLP_ERR_CUDA;
     if (vec) {
         // bulk copies: three 64 KB CTAs per SM
-        static bool attr_set[64] = {};
+        static std::atomic<bool> attr_set[64] = {};
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
-        if (!attr_set[dev]) {
+        if (!attr_set[dev].load()) {
+            // idempotent, so concurrent first calls may both set it
             if (cudaFuncSetAttribute(vocab_embedding_bulk_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, EMB_SMEM) != cudaSuccess)
                 return TPMLP_ERR_CUDA;
-            attr_set[dev] = true;
+            attr_set[dev].store(true);
         }
         const int64_t items = N * ((kp.row_bytes + EMB_CHUNK - 1) / EMB_CHUNK);
         const int64_t max_grid = (int64_t)device_sm_count() * 3;
