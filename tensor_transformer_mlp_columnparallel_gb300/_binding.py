@@ -159,7 +159,8 @@ def tpmlp_forward(X, W1, b1, W2, b2, Y, H, Z, act: str, mode: str, workspace=Non
     T = len(W1)
     N, D = X.shape
     Fs = W1[0].shape[1]
-    _require([X, b2, Y, workspace, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, None)
+    _require([X, b2, Y, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, X.dtype)
+    _require([workspace], X.device, None)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().tpmlp_forward(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X), _ptrs(W1),
                                _ptrs(b1), _ptrs(W2), _ptr(b2), _ptr(Y), _ptrs(H), _ptrs(Z),
@@ -173,7 +174,7 @@ def tpmlp_forward_noalloc(X, W1, b1, W2, b2, Y, H, Z, act: str):
     T = len(W1)
     N, D = X.shape
     Fs = W1[0].shape[1]
-    _require([X, b2, Y, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, None)
+    _require([X, b2, Y, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, X.dtype)
     _check(lib().tpmlp_forward_noalloc(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X),
                                        _ptrs(W1), _ptrs(b1), _ptrs(W2), _ptr(b2), _ptr(Y),
                                        _ptrs(H), _ptrs(Z), _stream(X)))
@@ -184,7 +185,8 @@ def tpmlp_swiglu_forward(X, Wg, Wu, Wd, Y, H, G, U, mode: str, workspace=None):
     T = len(Wg)
     N, D = X.shape
     Fs = Wg[0].shape[1]
-    _require([X, Y, workspace, *Wg, *Wu, *Wd, *H, *(G or []), *(U or [])], X.device, None)
+    _require([X, Y, *Wg, *Wu, *Wd, *H, *(G or []), *(U or [])], X.device, X.dtype)
+    _require([workspace], X.device, None)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().tpmlp_swiglu_forward(_dtype_code(X), N, D, Fs * T, T, _ptr(X), _ptrs(Wg),
                                       _ptrs(Wu), _ptrs(Wd), _ptr(Y), _ptrs(H), _ptrs(G), _ptrs(U),
@@ -196,8 +198,8 @@ def tpmlp_backward(X, W1, W2, H, Z, dY, dX, dW1, dW2, db1, db2, act: str, mode: 
     T = len(W1)
     N, D = X.shape
     Fs = W1[0].shape[1]
-    _require([X, dY, dX, db2, workspace, *W1, *W2, *H, *Z, *dW1, *dW2, *(db1 or [])], X.device,
-             None)
+    _require([X, dY, dX, db2, *W1, *W2, *H, *Z, *dW1, *dW2, *(db1 or [])], X.device, X.dtype)
+    _require([workspace], X.device, None)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().tpmlp_backward(_dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X), _ptrs(W1),
                                 _ptrs(W2), _ptrs(H), _ptrs(Z), _ptr(dY), _ptr(dX), _ptrs(dW1),
@@ -209,7 +211,8 @@ def tpmlp_block_reduce(partials: Sequence[torch.Tensor], b2, Y):
     """Y = sum_r partials[r] + b2, fp32 partials, Y fp32 or bf16."""
     T = len(partials)
     N, D = Y.shape
-    _require([*partials, b2, Y], Y.device, None)
+    _require([*partials], Y.device, torch.float32)
+    _require([b2, Y], Y.device, Y.dtype)
     for p in partials:
         if p.dtype != torch.float32:
             raise TypeError("partial sums are fp32")
@@ -221,7 +224,8 @@ def tpmlp_block_reduce_scatter(partials: Sequence[torch.Tensor], b2, Y_rows: Seq
     """Rows [r N/T, (r+1) N/T) of sum_r partials[r] + b2 into Y_rows[r]."""
     T = len(partials)
     N, D = partials[0].shape
-    _require([*partials, b2, *Y_rows], partials[0].device, None)
+    _require([*partials], partials[0].device, torch.float32)
+    _require([b2, *Y_rows], partials[0].device, Y_rows[0].dtype)
     _check(lib().tpmlp_block_reduce_scatter(_dtype_code(Y_rows[0]), N, D, T, _ptrs(partials),
                                             _ptr(b2), _ptrs(Y_rows), _stream(partials[0])))
 
@@ -232,7 +236,8 @@ def tpmlp_forward_reduce_scatter(X, W1, b1, W2, b2, Y_rows, H, Z, act: str, mode
     T = len(W1)
     N, D = X.shape
     Fs = W1[0].shape[1]
-    _require([X, b2, workspace, *Y_rows, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, None)
+    _require([X, b2, *Y_rows, *W1, *W2, *H, *(b1 or []), *(Z or [])], X.device, X.dtype)
+    _require([workspace], X.device, None)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().tpmlp_forward_reduce_scatter(
         _dtype_code(X), N, D, Fs * T, T, ACT[act], _ptr(X), _ptrs(W1), _ptrs(b1), _ptrs(W2),

@@ -398,6 +398,9 @@ def test_rejected_arguments_launch_nothing():
         tp.tpmlp_forward(X6, W16, None, W26, None, torch.empty(4, 6, device=dev()).bfloat16(), H,
                          None, "relu", "splitk")
     assert e.value.status == _binding.ERR_ALIGN
+    # mixed element types (fp32 weights with a bf16 input) are refused by the binding
+    with pytest.raises(TypeError):
+        tp.tpmlp_forward(X, [w.float() for w in W1], None, W2, None, Y, H, None, "relu", "splitk")
     assert tp.tpmlp_launch_count() == before
 
 
