@@ -4,8 +4,11 @@ must reproduce.
 Source: page "一层 MLP 太宽而放不下时怎样切？" (zwjcode.cn), §01 (H = act(X W1),
 Y = H W2), §05 (b2 added once; b1 follows the columns), §06 (backward:
 dW2 and dH local, dX = sum over column shards of dZ W1^T). The activation is
-ReLU or the tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear
-Units", 2016: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))).
+ReLU, the tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear
+Units", 2016: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))), or the exact
+(erf) GELU the pages' code uses (`nn.GELU()`, `F.gelu`, §01 and the course
+notes' FFN): z Phi(z) = 0.5 z (1 + erf(z / sqrt(2))), Phi the standard normal
+CDF; its derivative is Phi(z) + z phi(z), phi the standard normal density.
 
 Conventions taken where the pages are silent:
 - ReLU'(0) = 0 (strict z > 0), the usual autograd convention;
@@ -15,6 +18,7 @@ Conventions taken where the pages are silent:
 import math
 
 import numpy as np
+from scipy.special import erf
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
 GELU_CUBIC = 0.044715
@@ -37,6 +41,8 @@ def act(z, kind):
     if kind == "gelu_tanh":
         u = SQRT_2_OVER_PI * (z + GELU_CUBIC * z ** 3)
         return 0.5 * z * (1.0 + np.tanh(u))
+    if kind == "gelu_erf":
+        return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
     raise ValueError(kind)
 
 
@@ -50,6 +56,10 @@ def act_grad(z, kind):
         t = np.tanh(u)
         du = SQRT_2_OVER_PI * (1.0 + 3.0 * GELU_CUBIC * z ** 2)
         return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * du
+    if kind == "gelu_erf":
+        cdf = 0.5 * (1.0 + erf(z / math.sqrt(2.0)))
+        pdf = np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+        return cdf + z * pdf
     raise ValueError(kind)
 
 
