@@ -11,8 +11,16 @@
 
 namespace tpmlp {
 
+// Exact GELU (the pages' nn.GELU): z Phi(z), Phi(z) = (1 + erf(z / sqrt(2))) / 2,
+// derivative Phi(z) + z phi(z), phi(z) = exp(-z^2 / 2) / sqrt(2 pi); erf and
+// exp from CUDA's erff / expf (fp32 path) or erff / __expf (bf16 epilogue).
+__device__ __forceinline__ float gelu_erf_fwd(float z) {
+    return 0.5f * z * (1.f + erff(z * 0.7071067811865476f));
+}
+
 __device__ __forceinline__ float act_fwd(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
+    if (act == TPMLP_ACT_GELU_ERF) return gelu_erf_fwd(z);
     const float c = 0.7978845608028654f;   // sqrt(2/pi)
     const float u = c * fmaf(0.044715f * z, z * z, z);
     return 0.5f * z * (1.f + tanhf(u));
@@ -20,6 +28,8 @@ __device__ __forceinline__ float act_fwd(int act, float z) {
 
 __device__ __forceinline__ float act_grad(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    if (act == TPMLP_ACT_GELU_ERF)
+        return fmaf(z * 0.3989422804014327f, expf(-0.5f * z * z), 0.5f * (1.f + erff(z * 0.7071067811865476f)));
     const float c = 0.7978845608028654f;
     const float z2 = z * z;
     const float t = tanhf(c * fmaf(0.044715f * z, z2, z));
@@ -42,6 +52,7 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); 
 // magnitude either way). The fp32 path keeps the tanhf / expf forms above.
 __device__ __forceinline__ float act_fwd_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
+    if (act == TPMLP_ACT_GELU_ERF) return gelu_erf_fwd(z);
     const float c = 0.7978845608028654f;
     const float u = c * fmaf(0.044715f * z, z * z, z);
     const float e = __expf(fminf(-2.f * u, 80.f));
@@ -50,6 +61,8 @@ __device__ __forceinline__ float act_fwd_bf16(int act, float z) {
 
 __device__ __forceinline__ float act_grad_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    if (act == TPMLP_ACT_GELU_ERF)
+        return fmaf(z * 0.3989422804014327f, __expf(-0.5f * z * z), 0.5f * (1.f + erff(z * 0.7071067811865476f)));
     const float c = 0.7978845608028654f;
     const float z2 = z * z;
     const float u = c * fmaf(0.044715f * z, z2, z);

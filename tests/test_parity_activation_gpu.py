@@ -4,8 +4,8 @@ With X = I (N = D = 128) the column GEMM returns Z = W1 exactly, so the saved
 H is act(W1) entry by entry; with dY = e_0 rows and W2[:, 0] = 1 the hidden
 gradient dH is 1 everywhere, so dZ = act'(Z) and dW1 = X^T dZ = act'(W1).
 W1 holds 32768 bf16 values spread over [-12, 12], which covers both tails of
-GELU and the zero of GELU'. The oracle evaluates act and act' in float64 on
-the same (bf16-rounded) values.
+GELU (tanh and erf forms) and the zero of GELU'. The oracle evaluates act and
+act' in float64 on the same (bf16-rounded) values.
 
 Bounds (derived from the arithmetic, not fitted):
 - bf16 path: round-to-nearest bf16 of the fp32 result moves it by at most
@@ -14,6 +14,9 @@ Bounds (derived from the arithmetic, not fitted):
   absolute 2e-6 for the cancellation in act' near its zero (z ~ -0.75).
 - fp32 path (tanhf): relative 1e-5 plus an absolute 3e-6, the worst case of
   0.5 z (1 - t^2) u'(z) with t = tanhf(u) carrying a couple of ulps near 1.
+- the erf form (erff, a couple of ulps, on both paths) stays inside the same
+  bounds: its one cancellation, 1 + erf(z / sqrt(2)) in the negative tail,
+  costs at most ~1e-7 absolute after the factor z / 2.
 """
 
 import numpy as np
@@ -78,7 +81,7 @@ def shards_rows(W, st):
 
 
 @pytest.mark.parametrize("mode", ["splitk", "partials"])
-@pytest.mark.parametrize("act", ["gelu_tanh", "relu"])
+@pytest.mark.parametrize("act", ["gelu_tanh", "relu", "gelu_erf"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_act_and_act_grad_elementwise_over_both_tails(dtype, act, mode):
     st = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -120,3 +123,27 @@ def test_silu_elementwise_over_both_tails(dtype):
     assert torch.equal(torch.cat([g.float() for g in G], dim=1).cpu(), Zv)
     assert_elementwise(torch.cat([h.float() for h in H], dim=1),
                        oracle.mlp.silu(Zv.double().numpy()), dtype, "SiLU(z)")
+
+
+@pytest.mark.parametrize("mode", ["splitk", "partials"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_exact_gelu_block_forward_backward(dtype, mode):
+    """The pages' exact (erf) GELU through a whole block, ragged shapes."""
+    from tests.gpu_helpers import to_gpu, run_forward, run_backward, cat_cols, cat_rows
+    from tests.tolerance import assert_close
+    from workloads.gen import gen_random_mlp
+    inp = gen_random_mlp(N=200, D=264, F=2 * 520, T=2, dtype=dtype, act="gelu_erf", bias=True,
+                         seed=77)
+    gp = to_gpu(inp)
+    Y, H, Z = run_forward(gp, "gelu_erf", mode)
+    dX, dW1, dW2, db1, db2 = run_backward(gp, H, Z, "gelu_erf", mode, bias_grads=True)
+    torch.cuda.synchronize()
+    f = oracle.mlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_erf")
+    g = oracle.mlp.backward(inp.X, inp.W1, inp.b1, inp.W2, inp.dY, "gelu_erf")
+    assert_close(Y, f["Y"], dtype, "Y")
+    assert_close(cat_cols(H), f["H"], dtype, "H")
+    assert_close(dX, g["dX"], dtype, "dX")
+    assert_close(cat_cols(dW1), g["dW1"], dtype, "dW1")
+    assert_close(cat_rows(dW2), g["dW2"], dtype, "dW2")
+    assert_close(torch.cat([b.float() for b in db1]), g["db1"], dtype, "db1")
+    assert_close(db2, g["db2"], dtype, "db2")
