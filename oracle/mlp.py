@@ -8,7 +8,9 @@ ReLU, the tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear
 Units", 2016: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))), or the exact
 (erf) GELU the pages' code uses (`nn.GELU()`, `F.gelu`, §01 and the course
 notes' FFN): z Phi(z) = 0.5 z (1 + erf(z / sqrt(2))), Phi the standard normal
-CDF; its derivative is Phi(z) + z phi(z), phi the standard normal density.
+CDF; its derivative is Phi(z) + z phi(z), phi the standard normal density;
+or the sigmoid approximation of GELU on the interview page (`x / (1 +
+exp(-1.702 x))`): z s(z), s = sigmoid(1.702 z), derivative s (1 + 1.702 z (1 - s)).
 
 Conventions taken where the pages are silent:
 - ReLU'(0) = 0 (strict z > 0), the usual autograd convention;
@@ -22,6 +24,7 @@ from scipy.special import erf
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
 GELU_CUBIC = 0.044715
+GELU_SIGMOID_SCALE = 1.702
 
 
 def as_f64(a):
@@ -43,6 +46,8 @@ def act(z, kind):
         return 0.5 * z * (1.0 + np.tanh(u))
     if kind == "gelu_erf":
         return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+    if kind == "gelu_sigmoid":
+        return z / (1.0 + np.exp(-GELU_SIGMOID_SCALE * z))
     raise ValueError(kind)
 
 
@@ -60,6 +65,9 @@ def act_grad(z, kind):
         cdf = 0.5 * (1.0 + erf(z / math.sqrt(2.0)))
         pdf = np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
         return cdf + z * pdf
+    if kind == "gelu_sigmoid":
+        sg = 1.0 / (1.0 + np.exp(-GELU_SIGMOID_SCALE * z))
+        return sg * (1.0 + GELU_SIGMOID_SCALE * z * (1.0 - sg))
     raise ValueError(kind)
 
 

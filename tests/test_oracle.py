@@ -113,7 +113,7 @@ def test_column_dx_example():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
-@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf"])
+@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf", "gelu_sigmoid"])
 @pytest.mark.parametrize("bias", [False, True])
 def test_shard_sum_equals_unsharded(T, kind, bias):
     inp = gen_random_mlp(N=24, D=32, F=64, T=T, dtype="f32", act=kind, bias=bias, seed=3)
@@ -160,7 +160,7 @@ def test_block_reduce_worked_example_and_bias_once():
     np.testing.assert_array_equal(osh.block_reduce(parts, b2), arr(g["expected"]["Y"]) + b2)
 
 
-@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf"])
+@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf", "gelu_sigmoid"])
 def test_row_first_split_is_wrong(kind):
     rng = np.random.default_rng(0)
     X = rng.standard_normal((4, 8))
@@ -189,7 +189,7 @@ def _fd_case(kind, seed):
             return X, W1, b1, W2, b2, dY
 
 
-@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf"])
+@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf", "gelu_sigmoid"])
 def test_backward_matches_central_finite_differences(kind):
     X, W1, b1, W2, b2, dY = _fd_case(kind, 7)
     h = 1e-6
@@ -213,15 +213,19 @@ def test_backward_matches_central_finite_differences(kind):
         assert normwise_rel_err(g[name], num) <= 1e-6, name
 
 
-@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf"])
+@pytest.mark.parametrize("kind", ["relu", "gelu_tanh", "gelu_erf", "gelu_sigmoid"])
 @pytest.mark.parametrize("bias", [False, True])
 def test_backward_matches_torch_autograd(kind, bias):
     inp = gen_random_mlp(N=10, D=12, F=16, T=2, dtype="f32", act=kind, bias=bias, seed=2)
     t = {k: (None if v is None else v.double().clone().requires_grad_(True))
          for k, v in dict(X=inp.X, W1=inp.W1, b1=inp.b1, W2=inp.W2, b2=inp.b2).items()}
     Z = t["X"] @ t["W1"] + (t["b1"] if bias else 0.0)
-    H = (torch.relu(Z) if kind == "relu" else
-         torch.nn.functional.gelu(Z, approximate="tanh" if kind == "gelu_tanh" else "none"))
+    if kind == "relu":
+        H = torch.relu(Z)
+    elif kind == "gelu_sigmoid":
+        H = torch.nn.functional.silu(1.702 * Z) / 1.702
+    else:
+        H = torch.nn.functional.gelu(Z, approximate="tanh" if kind == "gelu_tanh" else "none")
     Y = H @ t["W2"] + (t["b2"] if bias else 0.0)
     dY = inp.dY.double()
     (Y * dY).sum().backward()
@@ -263,6 +267,22 @@ def test_gelu_erf_matches_torch_and_closed_forms():
     assert abs(omlp.act(10.0, "gelu_erf") - 10.0) < 1e-12
     # the erf and tanh forms are different functions (up to ~1e-3 apart)
     assert np.max(np.abs(omlp.act(zn, "gelu_erf") - omlp.act(zn, "gelu_tanh"))) > 1e-4
+
+
+def test_gelu_sigmoid_matches_scaled_silu_and_approximates_gelu():
+    """The interview page's sigmoid GELU equals SiLU(1.702 z) / 1.702 (torch's
+    silu and autograd in float64); act(0) = 0, act'(0) = 1/2; it stays within
+    0.021 of the exact GELU (the known accuracy of that approximation)."""
+    z = torch.linspace(-10, 10, 4001, dtype=torch.float64, requires_grad=True)
+    y = torch.nn.functional.silu(1.702 * z) / 1.702
+    y.sum().backward()
+    zn = z.detach().numpy()
+    np.testing.assert_allclose(omlp.act(zn, "gelu_sigmoid"), y.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(omlp.act_grad(zn, "gelu_sigmoid"), z.grad.numpy(), rtol=0, atol=1e-12)
+    assert omlp.act(0.0, "gelu_sigmoid") == 0.0
+    assert omlp.act_grad(0.0, "gelu_sigmoid") == 0.5
+    gap = np.max(np.abs(omlp.act(zn, "gelu_sigmoid") - omlp.act(zn, "gelu_erf")))
+    assert 0.01 < gap < 0.021
 
 
 def test_gelu_constant_mutation_is_detected(monkeypatch):
