@@ -65,8 +65,14 @@ typedef enum {
 
 /* RELU: max(z, 0), act'(0) = 0. GELU_TANH: 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3)))
  * (Hendrycks & Gimpel 2016). GELU_ERF: the exact form z Phi(z) = 0.5 z (1 + erf(z/sqrt(2)))
- * that the pages' code uses (nn.GELU(), F.gelu). act' is the exact derivative of each. */
-typedef enum { TPMLP_ACT_RELU = 0, TPMLP_ACT_GELU_TANH = 1, TPMLP_ACT_GELU_ERF = 2 } tpmlp_act;
+ * that the pages' code uses (nn.GELU(), F.gelu). GELU_SIGMOID: the interview page's
+ * approximation z / (1 + exp(-1.702 z)). act' is the exact derivative of each. */
+typedef enum {
+    TPMLP_ACT_RELU = 0,
+    TPMLP_ACT_GELU_TANH = 1,
+    TPMLP_ACT_GELU_ERF = 2,
+    TPMLP_ACT_GELU_SIGMOID = 3
+} tpmlp_act;
 typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
 
 /* How the T full-shape partial sums are combined (§04 block-end reduction).

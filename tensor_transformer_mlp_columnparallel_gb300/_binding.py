@@ -20,7 +20,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "tpmlp.h")
 
 MAX_SHARDS = 16
 OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
-ACT = {"relu": 0, "gelu_tanh": 1, "gelu_erf": 2}
+ACT = {"relu": 0, "gelu_tanh": 1, "gelu_erf": 2, "gelu_sigmoid": 3}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 MODE = {"partials": 0, "splitk": 1}
 OP_FORWARD, OP_BACKWARD = 0, 1

@@ -18,9 +18,15 @@ __device__ __forceinline__ float gelu_erf_fwd(float z) {
     return 0.5f * z * (1.f + erff(z * 0.7071067811865476f));
 }
 
+// Sigmoid approximation of GELU (interview page): z s, s = sigmoid(1.702 z),
+// derivative s (1 + 1.702 z (1 - s)) = s (1 + 1.702 z e s), e = exp(-1.702 z);
+// exponent clamped at 80 as in the forms below.
+constexpr float GELU_SIGMOID_SCALE = 1.702f;
+
 __device__ __forceinline__ float act_fwd(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
     if (act == TPMLP_ACT_GELU_ERF) return gelu_erf_fwd(z);
+    if (act == TPMLP_ACT_GELU_SIGMOID) return z / (1.f + expf(fminf(-GELU_SIGMOID_SCALE * z, 80.f)));
     const float c = 0.7978845608028654f;   // sqrt(2/pi)
     const float u = c * fmaf(0.044715f * z, z * z, z);
     return 0.5f * z * (1.f + tanhf(u));
@@ -30,6 +36,11 @@ __device__ __forceinline__ float act_grad(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     if (act == TPMLP_ACT_GELU_ERF)
         return fmaf(z * 0.3989422804014327f, expf(-0.5f * z * z), 0.5f * (1.f + erff(z * 0.7071067811865476f)));
+    if (act == TPMLP_ACT_GELU_SIGMOID) {
+        const float e = expf(fminf(-GELU_SIGMOID_SCALE * z, 80.f));
+        const float sg = 1.f / (1.f + e);
+        return sg * fmaf(GELU_SIGMOID_SCALE * z * e, sg, 1.f);
+    }
     const float c = 0.7978845608028654f;
     const float z2 = z * z;
     const float t = tanhf(c * fmaf(0.044715f * z, z2, z));
@@ -53,6 +64,7 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); 
 __device__ __forceinline__ float act_fwd_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? z : 0.f;
     if (act == TPMLP_ACT_GELU_ERF) return gelu_erf_fwd(z);
+    if (act == TPMLP_ACT_GELU_SIGMOID) return __fdividef(z, 1.f + __expf(fminf(-GELU_SIGMOID_SCALE * z, 80.f)));
     const float c = 0.7978845608028654f;
     const float u = c * fmaf(0.044715f * z, z * z, z);
     const float e = __expf(fminf(-2.f * u, 80.f));
@@ -63,6 +75,11 @@ __device__ __forceinline__ float act_grad_bf16(int act, float z) {
     if (act == TPMLP_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     if (act == TPMLP_ACT_GELU_ERF)
         return fmaf(z * 0.3989422804014327f, __expf(-0.5f * z * z), 0.5f * (1.f + erff(z * 0.7071067811865476f)));
+    if (act == TPMLP_ACT_GELU_SIGMOID) {
+        const float e = __expf(fminf(-GELU_SIGMOID_SCALE * z, 80.f));
+        const float sg = __fdividef(1.f, 1.f + e);
+        return sg * fmaf(GELU_SIGMOID_SCALE * z * e, sg, 1.f);
+    }
     const float c = 0.7978845608028654f;
     const float z2 = z * z;
     const float u = c * fmaf(0.044715f * z, z2, z);

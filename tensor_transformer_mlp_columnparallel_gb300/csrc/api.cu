@@ -135,7 +135,8 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 tpmlp_status check_dims(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act) {
     if (dt != TPMLP_F32 && dt != TPMLP_BF16) return TPMLP_ERR_DTYPE;
-    if (act != TPMLP_ACT_RELU && act != TPMLP_ACT_GELU_TANH && act != TPMLP_ACT_GELU_ERF)
+    if (act != TPMLP_ACT_RELU && act != TPMLP_ACT_GELU_TANH && act != TPMLP_ACT_GELU_ERF &&
+        act != TPMLP_ACT_GELU_SIGMOID)
         return TPMLP_ERR_ARG;
     if (N < 0) return TPMLP_ERR_ARG;
     if (D <= 0 || F <= 0 || T < 1 || T > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;

@@ -81,7 +81,7 @@ def shards_rows(W, st):
 
 
 @pytest.mark.parametrize("mode", ["splitk", "partials"])
-@pytest.mark.parametrize("act", ["gelu_tanh", "relu", "gelu_erf"])
+@pytest.mark.parametrize("act", ["gelu_tanh", "relu", "gelu_erf", "gelu_sigmoid"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_act_and_act_grad_elementwise_over_both_tails(dtype, act, mode):
     st = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -127,19 +127,21 @@ def test_silu_elementwise_over_both_tails(dtype):
 
 @pytest.mark.parametrize("mode", ["splitk", "partials"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_exact_gelu_block_forward_backward(dtype, mode):
-    """The pages' exact (erf) GELU through a whole block, ragged shapes."""
+@pytest.mark.parametrize("act", ["gelu_erf", "gelu_sigmoid"])
+def test_other_gelu_forms_block_forward_backward(dtype, mode, act):
+    """The pages' exact (erf) GELU and the interview page's sigmoid GELU
+    through a whole block, ragged shapes."""
     from tests.gpu_helpers import to_gpu, run_forward, run_backward, cat_cols, cat_rows
     from tests.tolerance import assert_close
     from workloads.gen import gen_random_mlp
-    inp = gen_random_mlp(N=200, D=264, F=2 * 520, T=2, dtype=dtype, act="gelu_erf", bias=True,
+    inp = gen_random_mlp(N=200, D=264, F=2 * 520, T=2, dtype=dtype, act=act, bias=True,
                          seed=77)
     gp = to_gpu(inp)
-    Y, H, Z = run_forward(gp, "gelu_erf", mode)
-    dX, dW1, dW2, db1, db2 = run_backward(gp, H, Z, "gelu_erf", mode, bias_grads=True)
+    Y, H, Z = run_forward(gp, act, mode)
+    dX, dW1, dW2, db1, db2 = run_backward(gp, H, Z, act, mode, bias_grads=True)
     torch.cuda.synchronize()
-    f = oracle.mlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_erf")
-    g = oracle.mlp.backward(inp.X, inp.W1, inp.b1, inp.W2, inp.dY, "gelu_erf")
+    f = oracle.mlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, act)
+    g = oracle.mlp.backward(inp.X, inp.W1, inp.b1, inp.W2, inp.dY, act)
     assert_close(Y, f["Y"], dtype, "Y")
     assert_close(cat_cols(H), f["H"], dtype, "H")
     assert_close(dX, g["dX"], dtype, "dX")

@@ -28,7 +28,7 @@ class MLPConfig:
     F: int
     T: int
     dtype: str          # "f32" or "bf16": storage type of X, W, b, H, Z, Y, grads
-    act: str            # "relu", "gelu_tanh" or "gelu_erf"
+    act: str            # "relu", "gelu_tanh", "gelu_erf" or "gelu_sigmoid"
     bias: bool
     backward: bool
     x_std: float
