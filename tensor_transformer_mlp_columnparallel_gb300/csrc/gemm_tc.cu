@@ -169,6 +169,20 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
     n0 = nt * BN;
 }
 
+// act / act' over one 32-column chunk with the activation fixed at compile
+// time, so the per-element code carries no activation branches
+template <int ACT>
+__device__ __forceinline__ void act_chunk(float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = act_fwd_bf16(ACT, v[j]);
+}
+
+template <int ACT>
+__device__ __forceinline__ void dact_chunk(float (&v)[32], const float (&z)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= act_grad_bf16(ACT, z[j]);
+}
+
 // Epilogue of one thread: 32 consecutive columns [col0, col0 + 32) of output
 // row `row`, accumulator values in r[].
 __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row, int col0, int M,
@@ -218,28 +232,34 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
                     if (col0 + j < N) z[j] = __float2bfloat16_rn(v[j]);
             }
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = act_fwd_bf16(e.act, v[j]);
+        switch (e.act) {   // one dispatch per chunk, a tight loop per activation
+            case TPMLP_ACT_RELU: act_chunk<TPMLP_ACT_RELU>(v); break;
+            case TPMLP_ACT_GELU_ERF: act_chunk<TPMLP_ACT_GELU_ERF>(v); break;
+            case TPMLP_ACT_GELU_SIGMOID: act_chunk<TPMLP_ACT_GELU_SIGMOID>(v); break;
+            default: act_chunk<TPMLP_ACT_GELU_TANH>(v); break;
+        }
     } else if (e.kind == EPI_DACT) {
         const __nv_bfloat16* z =
             static_cast<const __nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
+        float zv[32];
         if (full) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint4 w = *(reinterpret_cast<const uint4*>(z) + q);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float lo, hi;
-                    unpack_bf16x2(ws[h], lo, hi);
-                    v[q * 8 + 2 * h] *= act_grad_bf16(e.act, lo);
-                    v[q * 8 + 2 * h + 1] *= act_grad_bf16(e.act, hi);
-                }
+                unpack_bf16x2(w.x, zv[q * 8 + 0], zv[q * 8 + 1]);
+                unpack_bf16x2(w.y, zv[q * 8 + 2], zv[q * 8 + 3]);
+                unpack_bf16x2(w.z, zv[q * 8 + 4], zv[q * 8 + 5]);
+                unpack_bf16x2(w.w, zv[q * 8 + 6], zv[q * 8 + 7]);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < N) v[j] *= act_grad_bf16(e.act, bf2f(z[j]));
+            for (int j = 0; j < 32; ++j) zv[j] = col0 + j < N ? bf2f(z[j]) : 0.f;
+        }
+        switch (e.act) {
+            case TPMLP_ACT_RELU: dact_chunk<TPMLP_ACT_RELU>(v, zv); break;
+            case TPMLP_ACT_GELU_ERF: dact_chunk<TPMLP_ACT_GELU_ERF>(v, zv); break;
+            case TPMLP_ACT_GELU_SIGMOID: dact_chunk<TPMLP_ACT_GELU_SIGMOID>(v, zv); break;
+            default: dact_chunk<TPMLP_ACT_GELU_TANH>(v, zv); break;
         }
     }
     int cg = g;
