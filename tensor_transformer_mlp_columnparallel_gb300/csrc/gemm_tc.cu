@@ -3,7 +3,8 @@
 // One persistent CTA per SM, 6 warps with fixed roles:
 //   warp 0      TMA producer: streams A and B k-blocks into a STAGES-deep
 //               shared-memory ring (128-byte swizzled boxes), one mbarrier
-//               pair (full / empty) per stage;
+//               pair (full / empty) per stage; a stage is 64 deep in K, or
+//               128 (two 64-wide boxes per operand) for CTA pairs;
 //   warp 1      tensor-memory owner and MMA issuer: one thread issues
 //               tcgen05.mma (M = 128, N = BN, K = 16) into a TMEM accumulator
 //               and releases each stage with tcgen05.commit;
@@ -46,12 +47,11 @@ namespace tpmlp {
 namespace {
 
 constexpr int BM = 128;           // MMA M (rows of A / TMEM lanes)
-constexpr int BK = 64;            // one 128-byte swizzle row of bf16
+constexpr int BKB = 64;           // K extent of a K-major box: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;        // K of one kind::f16 MMA
 constexpr int NUM_THREADS = 192;
 constexpr int ACC_BUFS = 2;
 constexpr int BOX_MN = 64;        // MN extent of an MN-major box (128 bytes)
-constexpr int MN_BOX_BYTES = BOX_MN * BK * 2;   // 8 KB
 constexpr int GROUP_M = 8;        // raster band height, in M tiles
 constexpr int KSPLIT_ROWS = 64;   // rows a K-split cluster exchanges (M <= 64)
 
@@ -63,6 +63,15 @@ struct Cfg {
     static constexpr int CTAS = PAIR ? 2 : 1;
     static constexpr int TILE_M = BM * CTAS;
     static constexpr int B_ROWS = BN / CTAS;                 // B rows (N) staged per CTA
+    // K depth of one stage. A pair stages 128 (two 64-wide boxes per K-major
+    // operand, 3 stages of 64 KB) instead of 64 (7 of 32 KB): half the stage
+    // hand-offs per FLOP. On the power-capped fwd+bwd step (~1500 MHz) that
+    // took 2-3% fewer cycles; at 2070 MHz (zero data, uncapped) the shallower
+    // ring costs ~6% more. Single CTAs (few-token GEMMs) stage 64.
+    static constexpr int BK = PAIR ? 2 * BKB : BKB;
+    static constexpr int A_SUB = BM * BKB * 2;               // one K-major A box
+    static constexpr int B_SUB = B_ROWS * BKB * 2;           // one K-major B box
+    static constexpr int MN_BOX_BYTES = BOX_MN * BK * 2;     // one 64-wide MN chunk of a stage
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             // the pair's stage is complete when BOTH CTAs' bytes landed on the
             // even CTA's full barrier
             const uint32_t full0 = PAIR ? mapa_shared(bar(FULL), 0) : bar(FULL);
-            const int k_group = kb_per_group * BK;   // K extent of one shard
+            const int k_group = kb_per_group * C::BK;   // K extent of one shard
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
@@ -436,8 +445,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
                 // shard of the first k-block and its K offset inside the shard
                 int gk = p.fold ? kb_lo / kb_per_group : g;
-                int k0 = (p.fold ? kb_lo - (kb_lo / kb_per_group) * kb_per_group : kb_lo) * BK;
-                for (int kb = kb_lo; kb < kb_hi; ++kb, k0 += BK) {
+                int k0 = (p.fold ? kb_lo - (kb_lo / kb_per_group) * kb_per_group : kb_lo) * C::BK;
+                for (int kb = kb_lo; kb < kb_hi; ++kb, k0 += C::BK) {
                     if (k0 == k_group) {   // folded K loop: next shard
                         k0 = 0;
                         ++gk;
@@ -463,23 +472,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             tma_load_3d(dst, m, fb, x, y, z);
                     };
                     if (!p.a_mn) {
-                        load(a_dst, &p.tmA[gk], k0, am0);
+#pragma unroll
+                        for (int h = 0; h < C::BK / BKB; ++h)
+                            load(a_dst + h * C::A_SUB, &p.tmA[gk], k0 + h * BKB, am0);
                     } else if (p.a_3d) {
                         load3(a_dst, &p.tmA[gk], 0, k0, am0 / BOX_MN);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / BOX_MN; ++j)
-                            load(a_dst + j * MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
+                            load(a_dst + j * C::MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
                     }
                     // `rows` B rows (N index) starting at n_start from map m into dst
                     auto load_b = [&](uint32_t dst, const CUtensorMap* m, int n_start, int rows) {
                         if (!p.b_mn) {
-                            load(dst, m, k0, n_start);
+#pragma unroll
+                            for (int h = 0; h < C::BK / BKB; ++h)
+                                load(dst + h * C::B_SUB, m, k0 + h * BKB, n_start);
                         } else if (p.b_3d) {
                             load3(dst, m, 0, k0, n_start / BOX_MN);
                         } else {
                             for (int j = 0; j < rows / BOX_MN; ++j)
-                                load(dst + j * MN_BOX_BYTES, m, n_start + j * BOX_MN, k0);
+                                load(dst + j * C::MN_BOX_BYTES, m, n_start + j * BOX_MN, k0);
                         }
                     };
                     if (!p.dual) {
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         load_b(b_dst, rank == 0 ? &p.tmB[gk] : &p.tmB2[gk], n0 / 2, BN / 2);
                     } else {
                         load_b(b_dst, &p.tmB[gk], n0 / 2, BN / 2);
-                        load_b(b_dst + (BN / 2) * BK * 2, &p.tmB2[gk], n0 / 2, BN / 2);
+                        load_b(b_dst + (BN / 2) * (p.b_mn ? C::BK : BKB) * 2, &p.tmB2[gk], n0 / 2, BN / 2);
                     }
                     ++issued;
                     if (++s == C::STAGES) {
@@ -521,10 +534,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const uint32_t idesc = instr_desc(C::TILE_M, BN, p.a_mn, p.b_mn);
             // operand descriptors: K-major boxes advance 32 bytes per K=16 step,
             // MN-major boxes advance 16 rows of 128 bytes
-            const uint32_t a_lbo = p.a_mn ? MN_BOX_BYTES : 16;
-            const uint32_t b_lbo = p.b_mn ? MN_BOX_BYTES : 16;
+            const uint32_t a_lbo = p.a_mn ? C::MN_BOX_BYTES : 16;
+            const uint32_t b_lbo = p.b_mn ? C::MN_BOX_BYTES : 16;
             const uint32_t a_kstep = p.a_mn ? UMMA_K * 128 : UMMA_K * 2;
             const uint32_t b_kstep = p.b_mn ? UMMA_K * 128 : UMMA_K * 2;
+            // every 4 K steps: the next 64-wide K-major box (MN-major: 16 rows on)
+            const uint32_t a_sub = p.a_mn ? 4 * a_kstep : C::A_SUB;
+            const uint32_t b_sub = p.b_mn ? 4 * b_kstep : C::B_SUB;
             const uint64_t a_desc0 = smem_desc(sA0, a_lbo, 1024);
             const uint64_t b_desc0 = smem_desc(sB0, b_lbo, 1024);
             int s = 0;
@@ -550,9 +566,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     const uint64_t ad0 = a_desc0 + (uint64_t)((s * C::A_BYTES) >> 4);
                     const uint64_t bd0 = b_desc0 + (uint64_t)((s * C::B_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        const uint64_t ad = ad0 + (uint64_t)((k * a_kstep) >> 4);
-                        const uint64_t bd = bd0 + (uint64_t)((k * b_kstep) >> 4);
+                    for (int k = 0; k < C::BK / UMMA_K; ++k) {
+                        const uint64_t ad = ad0 + (uint64_t)(((k >> 2) * a_sub + (k & 3) * a_kstep) >> 4);
+                        const uint64_t bd = bd0 + (uint64_t)(((k >> 2) * b_sub + (k & 3) * b_kstep) >> 4);
                         if constexpr (PAIR)
                             tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else
@@ -759,16 +775,16 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
 
 // An MN-major operand ([K rows] x [mn columns], row pitch ld, mn % 64 == 0)
 // seen as 64-wide column chunks: dims {64, K, mn/64} with strides {ld*2, 128}
-// bytes. A box {64, BK, rows/64} lands in shared memory chunk by chunk, each
-// chunk BK rows of 128 bytes: the same layout as rows/64 separate 2-D boxes,
+// bytes. A box {64, bk, rows/64} lands in shared memory chunk by chunk, each
+// chunk bk rows of 128 bytes: the same layout as rows/64 separate 2-D boxes,
 // in one copy.
 bool make_map_mn_chunks(CUtensorMap* m, const void* base, int64_t mn, int64_t k, int64_t ld,
-                        int rows) {
+                        int rows, int bk) {
     auto fn = encode_fn();
     if (!fn || mn % BOX_MN != 0) return false;
     cuuint64_t dims[3] = {(cuuint64_t)BOX_MN, (cuuint64_t)k, (cuuint64_t)(mn / BOX_MN)};
     cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(BOX_MN * 2)};
-    cuuint32_t box[3] = {(cuuint32_t)BOX_MN, (cuuint32_t)BK, (cuuint32_t)(rows / BOX_MN)};
+    cuuint32_t box[3] = {(cuuint32_t)BOX_MN, (cuuint32_t)bk, (cuuint32_t)(rows / BOX_MN)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -831,25 +847,25 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     kp.a_3d = pr.a_mn && pr.M % BOX_MN == 0;
     kp.b_3d = pr.b_mn && pr.N % BOX_MN == 0;
     for (int g = 0; g < G && kp.a_3d; ++g)
-        kp.a_3d = make_map_mn_chunks(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BM);
+        kp.a_3d = make_map_mn_chunks(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BM, C::BK);
     for (int g = 0; g < G && kp.b_3d; ++g) {
-        kp.b_3d = make_map_mn_chunks(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, b_rows);
+        kp.b_3d = make_map_mn_chunks(&kp.tmB[g], pr.B[g], pr.N, pr.K, pr.ldb, b_rows, C::BK);
         if (kp.b_3d && pr.dual)
-            kp.b_3d = make_map_mn_chunks(&kp.tmB2[g], pr.B2[g], pr.N, pr.K, pr.ldb, b_rows);
+            kp.b_3d = make_map_mn_chunks(&kp.tmB2[g], pr.B2[g], pr.N, pr.K, pr.ldb, b_rows, C::BK);
     }
     for (int g = 0; g < G; ++g) {
         bool ok = true;
         if (!pr.a_mn)
-            ok = make_map(&kp.tmA[g], pr.A[g], pr.K, pr.M, pr.lda, BK, BM);
+            ok = make_map(&kp.tmA[g], pr.A[g], pr.K, pr.M, pr.lda, BKB, BM);
         else if (!kp.a_3d)
-            ok = make_map(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BOX_MN, BK);
+            ok = make_map(&kp.tmA[g], pr.A[g], pr.M, pr.K, pr.lda, BOX_MN, C::BK);
         for (int d = 0; d < (pr.dual ? 2 : 1); ++d) {
             CUtensorMap* m = d == 0 ? &kp.tmB[g] : &kp.tmB2[g];
             const void* b = d == 0 ? pr.B[g] : pr.B2[g];
             if (!pr.b_mn)
-                ok = ok && make_map(m, b, pr.K, pr.N, pr.ldb, BK, b_rows);
+                ok = ok && make_map(m, b, pr.K, pr.N, pr.ldb, BKB, b_rows);
             else if (!kp.b_3d)
-                ok = ok && make_map(m, b, pr.N, pr.K, pr.ldb, BOX_MN, BK);
+                ok = ok && make_map(m, b, pr.N, pr.K, pr.ldb, BOX_MN, C::BK);
         }
         if (!ok) return TPMLP_ERR_CUDA;
     }
@@ -863,7 +879,7 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     kp.m_tiles = (pr.M + C::TILE_M - 1) / C::TILE_M;
     kp.dual = pr.dual;
     kp.n_tiles = pr.dual ? (pr.N + BN / 2 - 1) / (BN / 2) : (pr.N + BN - 1) / BN;
-    kp.k_blocks = (pr.K + BK - 1) / BK;
+    kp.k_blocks = (pr.K + C::BK - 1) / C::BK;
     kp.num_tiles = (pr.fold ? 1 : G) * kp.m_tiles * kp.n_tiles;
     {
         bool shared_a = !pr.fold && G > 1, shared_b = !pr.fold && G > 1;
@@ -944,7 +960,7 @@ Plan choose_plan(const GemmProblem& pr) {
                           {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85}};
     const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
     const int groups = pr.fold ? 1 : pr.G;
-    const int64_t kb_total = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + 63) / 64);
+    const int64_t kb_total = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + BKB - 1) / BKB);
     double best = 1e300;
     int pick = 1;
     for (int i = 0; i < ncand; ++i) {
