@@ -175,16 +175,18 @@ class Block:
             self.dX = e(N, D)
             self.dW1 = [e(D, Fs) for _ in range(T)]
             self.dW2 = [e(Fs, D) for _ in range(T)]
-        wf = tp.tpmlp_workspace_bytes(0, dt, N, D, cfg.F, T, mode)
-        wb = tp.tpmlp_workspace_bytes(1, dt, N, D, cfg.F, T, mode) if with_dy else 0
+        # the balanced size also holds the few-token GEMMs' stream-K scratch
+        wf = tp.tpmlp_workspace_bytes_balanced(0, dt, N, D, cfg.F, T, mode)
+        wb = tp.tpmlp_workspace_bytes_balanced(1, dt, N, D, cfg.F, T, mode) if with_dy else 0
         self.ws = torch.empty(max(wf, wb, 256), dtype=torch.uint8, device=dev)
 
     def set_mode(self, mode):
         tp = self.tp
         cfg = self.cfg
         self.mode = mode
-        need = max(tp.tpmlp_workspace_bytes(0, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode),
-                   tp.tpmlp_workspace_bytes(1, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode), 256)
+        wsb = tp.tpmlp_workspace_bytes_balanced
+        need = max(wsb(0, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode),
+                   wsb(1, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode), 256)
         if self.ws.numel() < need:
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.dev)
 

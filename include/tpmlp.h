@@ -83,7 +83,9 @@ typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
  *   so the shard sum never leaves the tensor-core accumulator; b2 is added
  *   once in the epilogue. No workspace. (For N <= 64 tokens the (r, k) loop
  *   of a tile may be split across a cluster of 2-4 CTAs whose partial
- *   accumulators are added in on-chip shared memory; see tpmlp_gemm_plan.) */
+ *   accumulators are added in on-chip shared memory, or, given the optional
+ *   scratch of tpmlp_workspace_bytes_balanced, dealt out evenly to all SMs;
+ *   see tpmlp_gemm_plan.) */
 typedef enum { TPMLP_REDUCE_PARTIALS = 0, TPMLP_REDUCE_SPLITK = 1 } tpmlp_reduce_mode;
 
 typedef enum { TPMLP_OP_FORWARD = 0, TPMLP_OP_BACKWARD = 1 } tpmlp_op;
@@ -250,6 +252,25 @@ tpmlp_status tpmlp_forward_noalloc(tpmlp_dtype dt, int64_t N, int64_t D, int64_t
 size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
                              tpmlp_reduce_mode mode);
 
+/* Workspace bytes that also hold the optional scratch of the few-token
+ * GEMMs (bf16, 1 <= N <= 64; for other arguments the same as
+ * tpmlp_workspace_bytes). The scratch starts at round_up(required, 256)
+ * bytes: per-tile arrival counters and fp32 partial accumulators of up to
+ * 256 CTAs. Given a workspace of at least this size (16-byte aligned; for a
+ * SPLITK forward this is the only use of the workspace), the GEMMs whose M
+ * is the token count (the column GEMM, the row GEMM, dZ, dX) may run in the
+ * stream-K form: every SM streams the same number of k-blocks, and a tile
+ * whose K range two or more CTAs share is summed through the scratch, in
+ * CTA order, by the last CTA to finish it (no CTA waits for another; the
+ * result does not depend on timing). A smaller workspace (down to the
+ * required size) runs the same GEMMs without the scratch, with a different
+ * order of fp32 additions. The counters are reset on the call's stream
+ * before each use; what the scratch held before is never read.
+ * Returns (size_t)-1 for invalid shapes. Library extension; the source
+ * pages have no counterpart. */
+size_t tpmlp_workspace_bytes_balanced(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D,
+                                      int64_t F, int T, tpmlp_reduce_mode mode);
+
 /* Human-readable name of a status code (static string). */
 const char* tpmlp_status_str(tpmlp_status s);
 
@@ -276,16 +297,19 @@ tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * device for one GEMM of the block: M x N outputs per group, reduction
  * length K per group, G groups (shards), fold = 1 when the K loop runs over
  * all G groups into one output (the split-K shard sum), dual = 1 for the
- * gated GEMM (N counts outputs). Writes the tile's accumulator columns (128
- * or 256), the CTAs that issue one MMA (1, or 2 for a CTA pair) and the CTAs
- * of a cluster that share one tile's K range (1 = no split; used for folded
- * GEMMs with M <= 64, where the weights stream from HBM and the tiles are
- * fewer than the SMs). A query: launches nothing. Returns TPMLP_ERR_ARG for a null
- * output pointer, TPMLP_ERR_SHAPE for sizes < 1 or above 2^31 - 1 or G
- * outside [1, TPMLP_MAX_SHARDS], TPMLP_ERR_CUDA when the device queries fail.
- * Library introspection; the source pages have no counterpart. */
-tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, int dual, int* bn,
-                             int* mma_ctas, int* ksplit);
+ * gated GEMM (N counts outputs), balanced = 1 when the call's workspace holds
+ * the few-token scratch (tpmlp_workspace_bytes_balanced). Writes the tile's
+ * accumulator columns (128 or 256), the CTAs that issue one MMA (1, or 2 for
+ * a CTA pair) and the K split: the CTAs of a cluster that share one tile's
+ * K range (1 = no split; 2-4 for folded GEMMs with M <= 64, where the weights
+ * stream from HBM and the tiles are fewer than the SMs), or 0 for the
+ * stream-K form (M <= 64 with the scratch). A query: launches nothing.
+ * Returns TPMLP_ERR_ARG for a null output pointer, TPMLP_ERR_SHAPE for sizes
+ * < 1 or above 2^31 - 1 or G outside [1, TPMLP_MAX_SHARDS], TPMLP_ERR_CUDA
+ * when the device queries fail. Library introspection; the source pages
+ * have no counterpart. */
+tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, int dual,
+                             int balanced, int* bn, int* mma_ctas, int* ksplit);
 
 /* Number of kernels this library has launched in this process. */
 int64_t tpmlp_launch_count(void);

@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     tpmlp_vocab_ce_backward,
     tpmlp_vocab_embedding,
     tpmlp_workspace_bytes,
+    tpmlp_workspace_bytes_balanced,
 )
 
 
@@ -57,7 +58,7 @@ def mlp_forward(X: torch.Tensor, W1: Sequence[torch.Tensor], W2: Sequence[torch.
     Z = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_z else None
     if workspace is None:
         workspace = _workspace(
-            tpmlp_workspace_bytes(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
+            tpmlp_workspace_bytes_balanced(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
     tpmlp_forward(X, list(W1), list(b1) if b1 is not None else None, list(W2), b2, Y, H, Z,
                   act, mode, workspace)
     return Y, H, Z
@@ -78,7 +79,7 @@ def mlp_backward(X, W1, W2, H, Z, dY, act: str = "gelu_tanh", mode: str = "split
     db2 = torch.empty((D,), dtype=dt, device=dev) if bias_grads else None
     if workspace is None:
         workspace = _workspace(
-            tpmlp_workspace_bytes(_binding.OP_BACKWARD, dt, N, D, Fs * T, T, mode), dev)
+            tpmlp_workspace_bytes_balanced(_binding.OP_BACKWARD, dt, N, D, Fs * T, T, mode), dev)
     tpmlp_backward(X, list(W1), list(W2), list(H), list(Z), dY, dX, dW1, dW2, db1, db2, act, mode,
                    workspace)
     return dX, dW1, dW2, db1, db2
@@ -123,7 +124,7 @@ def mlp_forward_reduce_scatter(X, W1, W2, b1=None, b2=None, act: str = "gelu_tan
     Y_rows = [torch.empty((N // T, D), dtype=dt, device=dev) for _ in range(T)]
     H = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)]
     Z = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_z else None
-    ws = _workspace(tpmlp_workspace_bytes(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
+    ws = _workspace(tpmlp_workspace_bytes_balanced(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
     tpmlp_forward_reduce_scatter(X, list(W1), list(b1) if b1 is not None else None, list(W2), b2,
                                  Y_rows, H, Z, act, mode, ws)
     return Y_rows, H, Z
@@ -146,6 +147,6 @@ def swiglu_forward(X, Wg, Wu, Wd, mode: str = "splitk", save_gate_up: bool = Fal
     H = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)]
     G = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_gate_up else None
     U = [torch.empty((N, Fs), dtype=dt, device=dev) for _ in range(T)] if save_gate_up else None
-    ws = _workspace(tpmlp_workspace_bytes(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
+    ws = _workspace(tpmlp_workspace_bytes_balanced(_binding.OP_FORWARD, dt, N, D, Fs * T, T, mode), dev)
     tpmlp_swiglu_forward(X, list(Wg), list(Wu), list(Wd), Y, H, G, U, mode, ws)
     return Y, H, G, U

@@ -61,13 +61,15 @@ _SIGNATURES = {
     "tpmlp_vocab_ce": (_int, [_i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tpmlp_vocab_ce_backward": (_int, [_i64, _i64, _int, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "tpmlp_workspace_bytes": (ctypes.c_size_t, [_int, _int, _i64, _i64, _i64, _int, _int]),
+    "tpmlp_workspace_bytes_balanced": (ctypes.c_size_t, [_int, _int, _i64, _i64, _i64, _int, _int]),
     "tpmlp_status_str": (ctypes.c_char_p, [_int]),
     "tpmlp_check_device_error": (_int, [_vp]),
     "tpmlp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "tpmlp_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "tpmlp_launch_count": (ctypes.c_int64, []),
     "tpmlp_gemm_plan": (_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _int, _int, _int,
-                               ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+                               _int, ctypes.POINTER(_int), ctypes.POINTER(_int),
+                               ctypes.POINTER(_int)]),
     "tpmlp_timing_enable": (None, [_int]),
     "tpmlp_timing_read": (_int, [ctypes.POINTER(KernelTiming), _int]),
     "tpmlp_timing_reset": (None, []),
@@ -151,6 +153,13 @@ def _require(ts, device, dtype):
 def tpmlp_workspace_bytes(op: int, dtype: torch.dtype, N: int, D: int, F: int, T: int,
                           mode: str) -> int:
     return int(lib().tpmlp_workspace_bytes(op, DTYPE[dtype], N, D, F, T, MODE[mode]))
+
+
+def tpmlp_workspace_bytes_balanced(op: int, dtype: torch.dtype, N: int, D: int, F: int, T: int,
+                                   mode: str) -> int:
+    """Workspace size that also holds the few-token GEMMs' stream-K scratch
+    (see include/tpmlp.h)."""
+    return int(lib().tpmlp_workspace_bytes_balanced(op, DTYPE[dtype], N, D, F, T, MODE[mode]))
 
 
 def tpmlp_forward(X, W1, b1, W2, b2, Y, H, Z, act: str, mode: str, workspace=None):
@@ -298,12 +307,15 @@ def tpmlp_launch_count() -> int:
     return int(lib().tpmlp_launch_count())
 
 
-def tpmlp_gemm_plan(M: int, N: int, K: int, G: int, fold: bool = False, dual: bool = False):
+def tpmlp_gemm_plan(M: int, N: int, K: int, G: int, fold: bool = False, dual: bool = False,
+                    balanced: bool = False):
     """Launch configuration of the bf16 tensor-core GEMM for this shape on the
-    current device: (accumulator columns, CTAs per MMA, K-split cluster size)."""
+    current device: (accumulator columns, CTAs per MMA, K split: cluster size,
+    or 0 for stream-K, which needs balanced=True)."""
     bn, ctas, ks = _int(0), _int(0), _int(0)
     _check(lib().tpmlp_gemm_plan(M, N, K, G, 1 if fold else 0, 1 if dual else 0,
-                                 ctypes.byref(bn), ctypes.byref(ctas), ctypes.byref(ks)))
+                                 1 if balanced else 0, ctypes.byref(bn), ctypes.byref(ctas),
+                                 ctypes.byref(ks)))
     return bn.value, ctas.value, ks.value
 
 

@@ -173,7 +173,48 @@ size_t dz_bytes(tpmlp_dtype dt, int64_t N, int64_t Fs, int T) {
     return (size_t)T * round256((size_t)N * Fs * (dt == TPMLP_BF16 ? 2 : 4));
 }
 
-tpmlp_status run_gemm(tpmlp_dtype dt, const GemmProblem& p, cudaStream_t s) {
+// Optional scratch of the few-token (N <= 64) bf16 GEMMs' stream-K form: two
+// arrival counters per tile for the most tiles any GEMM of the block has
+// (T groups of up to max(F/T, D) columns in 128-column tiles), then the
+// partial-accumulator slots.
+size_t sk_cnt_bytes(int64_t D, int64_t Fs, int T) {
+    const int64_t cols = Fs > D ? Fs : D;
+    return round256((size_t)2 * T * ((cols + 127) / 128) * sizeof(int));
+}
+size_t sk_bytes(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T) {
+    if (dt != TPMLP_BF16 || N < 1 || N > 64) return 0;
+    return sk_cnt_bytes(D, F / T, T) + sk_part_bytes_for(N);
+}
+
+struct SkArea {
+    float* part = nullptr;
+    size_t part_bytes = 0;
+    int* cnt = nullptr;
+    int64_t cnt_cap = 0;
+};
+
+// The stream-K scratch at round256(base) bytes into the workspace, if the
+// caller's workspace is that large (see tpmlp_workspace_bytes_balanced).
+SkArea sk_area(void* ws, size_t ws_bytes, size_t base, tpmlp_dtype dt, int64_t N, int64_t D,
+               int64_t F, int T) {
+    SkArea a;
+    const size_t need = sk_bytes(dt, N, D, F, T);
+    const size_t off = round256(base);
+    if (need == 0 || ws == nullptr || !aligned16(ws) || ws_bytes < off + need) return a;
+    char* p = static_cast<char*>(ws) + off;
+    const size_t cb = sk_cnt_bytes(D, F / T, T);
+    a.cnt = reinterpret_cast<int*>(p);
+    a.cnt_cap = (int64_t)(cb / sizeof(int));
+    a.part = reinterpret_cast<float*>(p + cb);
+    a.part_bytes = need - cb;
+    return a;
+}
+
+tpmlp_status run_gemm(tpmlp_dtype dt, GemmProblem p, cudaStream_t s, const SkArea& sk = SkArea()) {
+    p.sk_part = sk.part;
+    p.sk_part_bytes = sk.part_bytes;
+    p.sk_cnt = sk.cnt;
+    p.sk_cnt_cap = sk.cnt_cap;
     return dt == TPMLP_BF16 ? run_gemm_tc(p, s) : run_gemm_simt(p, s);
 }
 
@@ -212,12 +253,20 @@ size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, 
     return (size_t)-1;
 }
 
+size_t tpmlp_workspace_bytes_balanced(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F,
+                                      int T, tpmlp_reduce_mode mode) {
+    const size_t base = tpmlp_workspace_bytes(op, dt, N, D, F, T, mode);
+    if (base == (size_t)-1) return base;
+    const size_t sk = sk_bytes(dt, N, D, F, T);
+    return sk == 0 ? base : round256(base) + sk;
+}
+
 // Row shards and the block-end sum (§02-§05): Y = sum_r H^(r) W2^(r) + b2, into
 // Y or, with Y_rows, row block r of Y into Y_rows[r].
 static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int Fs,
                               const void* const* H, const void* const* W2, const void* b2,
                               void* Y, void* const* Y_rows, tpmlp_reduce_mode mode,
-                              void* workspace, cudaStream_t s) {
+                              void* workspace, cudaStream_t s, const SkArea& sk) {
     const int f32 = dt == TPMLP_BF16 ? 0 : 1;
     if (mode == TPMLP_REDUCE_PARTIALS) {
         const size_t stride = round256((size_t)N * D * 4);
@@ -233,7 +282,7 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
             row.epi.C[r] = pr;
             parts[r] = pr;
         }
-        TPMLP_TRY(run_gemm(dt, row, s));
+        TPMLP_TRY(run_gemm(dt, row, s, sk));
         TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, b2, Y, s,
                                    Y_rows ? "block_reduce_scatter_bias" : "block_reduce_bias",
                                    Y_rows));
@@ -254,7 +303,7 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
             row.A[r] = H[r];
             row.B[r] = W2[r];
         }
-        TPMLP_TRY(run_gemm(dt, row, s));
+        TPMLP_TRY(run_gemm(dt, row, s, sk));
     }
     return TPMLP_OK;
 }
@@ -307,11 +356,12 @@ static tpmlp_status forward_impl(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F
         col.epi.bias[r] = b1 ? b1[r] : nullptr;
         col.epi.aux[r] = Z ? Z[r] : nullptr;
     }
-    TPMLP_TRY(run_gemm(dt, col, s));
+    const SkArea sk = sk_area(workspace, workspace_bytes, need, dt, N, D, F, T);
+    TPMLP_TRY(run_gemm(dt, col, s, sk));
 
     // 2. row shards and the block-end sum
     return block_end(dt, N, D, T, Fs, reinterpret_cast<const void* const*>(H), W2, b2, Y, Y_rows,
-                     mode, workspace, s);
+                     mode, workspace, s, sk);
 }
 
 tpmlp_status tpmlp_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
@@ -374,10 +424,11 @@ tpmlp_status tpmlp_swiglu_forward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t 
         col.epi.aux[r] = G ? G[r] : nullptr;
         col.epi.aux2[r] = U ? U[r] : nullptr;
     }
-    TPMLP_TRY(run_gemm(dt, col, s));
+    const SkArea sk = sk_area(workspace, workspace_bytes, need, dt, N, D, F, T);
+    TPMLP_TRY(run_gemm(dt, col, s, sk));
     // 2. the down projection's row shards and the block-end sum, as in the plain block
     return block_end(dt, N, D, T, Fs, reinterpret_cast<const void* const*>(H), Wd, nullptr, Y,
-                     nullptr, mode, workspace, s);
+                     nullptr, mode, workspace, s, sk);
 }
 
 tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T, tpmlp_act act,
@@ -405,6 +456,10 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
         if (workspace == nullptr || workspace_bytes < need) return TPMLP_ERR_WORKSPACE;
         if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
     }
+    const SkArea sk =
+        N > 0 ? sk_area(workspace, workspace_bytes,
+                        tpmlp_workspace_bytes(TPMLP_OP_BACKWARD, dt, N, D, F, T, mode), dt, N, D, F, T)
+              : SkArea();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Fs = (int)(F / T);
     const int f32 = bf ? 0 : 1;
@@ -440,7 +495,7 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
         g1.epi.C[r] = dZ[r];
         g1.epi.aux[r] = const_cast<void*>(Z[r]);
     }
-    TPMLP_TRY(run_gemm(dt, g1, s));
+    TPMLP_TRY(run_gemm(dt, g1, s, sk));
 
     // 2. dW2^(r) = H^(r)^T dY: A(m, k) = H^(r)[k, m] (MN-major), B(k, n) = dY[k, n]
     GemmProblem g2 = problem(Fs, (int)D, (int)N, T, 0, Fs, 1, D, 1, "bwd_dw2_gemm");
@@ -482,7 +537,7 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
             g4.epi.C[r] = pr;
             parts[r] = pr;
         }
-        TPMLP_TRY(run_gemm(dt, g4, s));
+        TPMLP_TRY(run_gemm(dt, g4, s, sk));
         TPMLP_TRY(run_block_reduce(f32, N, D, T, parts, nullptr, dX, s, "block_reduce_dx"));
     } else {
         GemmProblem g4 = problem((int)N, (int)D, Fs, T, 1, Fs, 0, Fs, 0, "bwd_dx_gemm_splitk");
@@ -494,7 +549,7 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
             g4.A[r] = dZ[r];
             g4.B[r] = W1[r];
         }
-        TPMLP_TRY(run_gemm(dt, g4, s));
+        TPMLP_TRY(run_gemm(dt, g4, s, sk));
     }
 
     // 5. bias gradients
@@ -573,14 +628,24 @@ tpmlp_status tpmlp_vocab_ce_backward(int64_t N, int64_t V, int T, const float* l
                                  static_cast<cudaStream_t>(stream));
 }
 
-tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, int dual, int* bn,
-                             int* mma_ctas, int* ksplit) {
+tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, int dual,
+                             int balanced, int* bn, int* mma_ctas, int* ksplit) {
     if (bn == nullptr || mma_ctas == nullptr || ksplit == nullptr) return TPMLP_ERR_ARG;
     const int64_t lim = 2147483647;
     if (M < 1 || N < 1 || K < 1 || M > lim || N > lim || K > lim || G < 1 || G > TPMLP_MAX_SHARDS)
         return TPMLP_ERR_SHAPE;
     GemmProblem p = problem((int)M, (int)N, (int)K, G, fold ? 1 : 0, K, 0, K, 0, "plan");
     p.dual = dual ? 1 : 0;
+    if (balanced && M <= 64) {
+        // a scratch as large as the block's workspace would provide (never
+        // dereferenced: the plan launches nothing)
+        static float part_dummy;
+        static int cnt_dummy;
+        p.sk_part = &part_dummy;
+        p.sk_part_bytes = sk_part_bytes_for(M);
+        p.sk_cnt = &cnt_dummy;
+        p.sk_cnt_cap = (int64_t)2 * G * ((N + 127) / 128);
+    }
     return plan_gemm_tc(p, bn, mma_ctas, ksplit);
 }
 

@@ -108,6 +108,11 @@ struct TcParams {
     int band;         // band width in tiles
     int ksplit;       // CTAs of a cluster sharing one tile's K range (single-CTA
                       // tiles, M <= KSPLIT_ROWS, one tile per cluster); 1 = off
+    int sk;           // 1: stream-K (see Work)
+    int sk_units;     // U = tiles x k-blocks
+    int sk_rows;      // rows of a scratch slot (32 or 64)
+    float* sk_part;   // P x 2 slots of sk_rows x BN fp32 partial accumulators
+    int* sk_cnt;      // 2 counters per tile (one per 32 rows), zero at launch
     EpiArgs epi;
     int* err;
     uint64_t timeout_ns;
@@ -176,6 +181,54 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
     }
     m0 = mt * TILE_M;
     n0 = nt * BN;
+}
+
+// The work items of one CTA: tiles first_tile, first_tile + step, ... with
+// the k-block range [kb_lo, kb_hi) each, or, with stream-K (few-token GEMMs:
+// single-CTA tiles, M <= KSPLIT_ROWS), the CTA's contiguous range
+// [i U / P, (i+1) U / P) of the U = tiles x k-blocks, cut at tile
+// boundaries. Every role walks the same sequence.
+struct Work {
+    int t, kb0, kb1;   // current item: tile, k-blocks [kb0, kb1)
+    int u, u_end;      // stream-K: next unit, end of the CTA's units
+    int kb_total, step, ntiles;
+    bool sk;
+    __device__ __forceinline__ Work(const TcParams& p, int first_tile, int tile_step, int kb_lo,
+                                    int kb_hi, int kbt)
+        : t(first_tile), kb0(kb_lo), kb1(kb_hi), u(0), u_end(0), kb_total(kbt), step(tile_step),
+          ntiles(p.num_tiles), sk(p.sk != 0) {
+        if (sk) {
+            u = (int)((int64_t)blockIdx.x * p.sk_units / gridDim.x);
+            u_end = (int)((int64_t)(blockIdx.x + 1) * p.sk_units / gridDim.x);
+            load();
+        }
+    }
+    __device__ __forceinline__ void load() {
+        if (u < u_end) {
+            t = u / kb_total;
+            kb0 = u - t * kb_total;
+            kb1 = min(kb_total, kb0 + (u_end - u));
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return sk ? u < u_end : t < ntiles; }
+    __device__ __forceinline__ void next() {
+        if (sk) {
+            u += kb1 - kb0;
+            load();
+        } else {
+            t += step;
+        }
+    }
+    // a stream-K item that covers only part of its tile's K range
+    __device__ __forceinline__ bool partial() const { return sk && (kb0 > 0 || kb1 < kb_total); }
+};
+
+// stream-K: the CTA whose range holds unit x, and the tile of CTA c's first unit
+__device__ __forceinline__ int sk_cta_of(int64_t x, int64_t U, int P) {
+    return (int)(((x + 1) * P - 1) / U);
+}
+__device__ __forceinline__ int sk_first_tile(int c, int64_t U, int P, int kb_total) {
+    return (int)((int64_t)c * U / P / kb_total);
 }
 
 // act / act' over one 32-column chunk with the activation fixed at compile
@@ -438,15 +491,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
+            for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); ok && w.valid(); w.next()) {
+                const int t = w.t;
                 int g, m0, n0;
                 decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
                 const int am0 = m0 + (int)rank * BM;          // this CTA's A rows
                 const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
                 // shard of the first k-block and its K offset inside the shard
-                int gk = p.fold ? kb_lo / kb_per_group : g;
-                int k0 = (p.fold ? kb_lo - (kb_lo / kb_per_group) * kb_per_group : kb_lo) * C::BK;
-                for (int kb = kb_lo; kb < kb_hi; ++kb, k0 += C::BK) {
+                int gk = p.fold ? w.kb0 / kb_per_group : g;
+                int k0 = (p.fold ? w.kb0 - (w.kb0 / kb_per_group) * kb_per_group : w.kb0) * C::BK;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, k0 += C::BK) {
                     if (k0 == k_group) {   // folded K loop: next shard
                         k0 = 0;
                         ++gk;
@@ -548,14 +602,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < p.num_tiles; t += tile_step) {
+            for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); ok && w.valid(); w.next()) {
                 if (!wait_fast(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = kb_lo; kb < kb_hi; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_fast(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
@@ -569,10 +623,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     for (int k = 0; k < C::BK / UMMA_K; ++k) {
                         const uint64_t ad = ad0 + (uint64_t)(((k >> 2) * a_sub + (k & 3) * a_kstep) >> 4);
                         const uint64_t bd = bd0 + (uint64_t)(((k >> 2) * b_sub + (k & 3) * b_kstep) >> 4);
+                        const uint32_t accum = ((kb - w.kb0) | k) != 0 ? 1u : 0u;
                         if constexpr (PAIR)
-                            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
                         else
-                            tc_mma_f16(d_tmem, ad, bd, idesc, ((kb - kb_lo) | k) != 0 ? 1u : 0u);
+                            tc_mma_f16(d_tmem, ad, bd, idesc, accum);
                     }
                     // frees stage s in both CTAs once these MMAs have read it
                     if constexpr (PAIR)
@@ -609,7 +664,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         int acc = 0;
         uint32_t aph = 0;
         uint32_t rph = 0;   // K split: phase of the exchange barriers
-        for (int t = first_tile; t < p.num_tiles; t += tile_step) {
+        for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); w.valid(); w.next()) {
+            const int t = w.t;
             int g, m0, n0;
             decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
             // one lane waits; the warp stays converged for the .sync.aligned TMEM loads
@@ -620,6 +676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             if (!ok) break;
             tc_fence_after();
             const int row = m0 + (int)rank * BM + quarter * 32 + lane;
+            bool released = false;   // this warp's TEMPTY arrival for the item is done
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if (ks > 1) {
@@ -632,7 +689,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 // and run the epilogue.
                 const bool xfer = quarter < red_warps;           // warp holds rows < 64
                 const uint32_t rrow = (uint32_t)(quarter * 32 + lane);
-                const bool has_k = kb_hi > kb_lo;
+                const bool has_k = w.kb1 > w.kb0;
                 if (krank == 0) {
                     if (warp == 2 && lane == 0)
                         for (int j = 1; j < ks; ++j) mbar_arrive_cluster(mapa_shared(bar(RFREE), (uint32_t)j));
@@ -690,6 +747,100 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     mbar_arrive_cluster(mapa_shared(bar(RFULL), 0u));   // release: this lane's stores
                 }
                 rph ^= 1u;
+            } else if (w.partial()) {
+                // Stream-K: this CTA accumulated k-blocks [kb0, kb1) of the
+                // tile. Each warp holding live rows stores its partial rows in
+                // the CTA's scratch slot for the tile (one for its first tile,
+                // one for its last) and counts itself in on the tile's
+                // counter for those rows; the warp that arrives last sums the
+                // slots of all CTAs sharing the tile in CTA order (the same
+                // order whichever warp is last, so the result does not depend
+                // on timing) and runs the epilogue. Nothing waits.
+                if (quarter < red_warps) {
+                    const int P = (int)gridDim.x;
+                    const int64_t U = p.sk_units;
+                    const int rrow = quarter * 32 + lane;
+                    // the CTAs c_first .. c_first + n_contrib - 1 share the tile
+                    const int c_first = sk_cta_of((int64_t)t * kb_total, U, P);
+                    const int n_contrib = sk_cta_of((int64_t)(t + 1) * kb_total - 1, U, P) - c_first + 1;
+                    auto slot = [&](int k) -> float4* {
+                        const int cta = c_first + k;
+                        const int idx = 2 * cta + (sk_first_tile(cta, U, P, kb_total) == t ? 0 : 1);
+                        return reinterpret_cast<float4*>(p.sk_part + (size_t)idx * p.sk_rows * BN);
+                    };
+                    float4* mine = slot((int)blockIdx.x - c_first);
+                    for (int c = 0; c < BN; c += 32) {
+                        if (n0 + c >= p.N) break;
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32cols(tbase + (uint32_t)c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            mine[(c / 4 + q) * p.sk_rows + rrow] =
+                                make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    }
+                    // the accumulator is read: hand it back to the MMA before
+                    // the count and the sum (global memory only from here)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+                    released = true;
+                    // release: every lane's partial rows before the count
+                    __threadfence();
+                    __syncwarp();
+                    int last = 0;
+                    if (lane == 0) {
+                        __threadfence();
+                        last = atomicAdd(p.sk_cnt + 2 * t + quarter, 1) == n_contrib - 1;
+                        if (last) __threadfence();   // acquire: the other partials
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    __syncwarp();
+                    if (last) {
+                        for (int c = 0; c < BN; c += 32) {
+                            if (n0 + c >= p.N) break;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                            // four slots' loads in flight at a time; the sum
+                            // still adds the slots in order k = 0, 1, ...
+                            int k = 0;
+                            for (; k + 4 <= n_contrib; k += 4) {
+                                const float4* s0 = slot(k);
+                                const float4* s1 = slot(k + 1);
+                                const float4* s2 = slot(k + 2);
+                                const float4* s3 = slot(k + 3);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const int o = (c / 4 + q) * p.sk_rows + rrow;
+                                    const float4 x0 = __ldcg(s0 + o), x1 = __ldcg(s1 + o);
+                                    const float4 x2 = __ldcg(s2 + o), x3 = __ldcg(s3 + o);
+                                    v[4 * q + 0] = (((v[4 * q + 0] + x0.x) + x1.x) + x2.x) + x3.x;
+                                    v[4 * q + 1] = (((v[4 * q + 1] + x0.y) + x1.y) + x2.y) + x3.y;
+                                    v[4 * q + 2] = (((v[4 * q + 2] + x0.z) + x1.z) + x2.z) + x3.z;
+                                    v[4 * q + 3] = (((v[4 * q + 3] + x0.w) + x1.w) + x2.w) + x3.w;
+                                }
+                            }
+                            for (; k < n_contrib; ++k) {
+                                const float4* sl = slot(k);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 x = __ldcg(sl + (c / 4 + q) * p.sk_rows + rrow);
+                                    v[4 * q + 0] += x.x;
+                                    v[4 * q + 1] += x.y;
+                                    v[4 * q + 2] += x.z;
+                                    v[4 * q + 3] += x.w;
+                                }
+                            }
+                            uint32_t r[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+                            epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                        }
+                    }
+                }
             } else if (!p.dual) {
                 for (int c = 0; c < BN; c += 32) {
                     if (n0 + c >= p.N) break;
@@ -711,13 +862,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     epilogue_swiglu_chunk(p.epi, g, row, n0o + c, p.M, p.N, rg, ru);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR)
-                    mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
-                else
-                    mbar_arrive(bar(TEMPTY + acc));
+            if (!released) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+                    else
+                        mbar_arrive(bar(TEMPTY + acc));
+                }
             }
             if (++acc == ACC_BUFS) {
                 acc = 0;
@@ -830,8 +983,33 @@ int resident_units(int cl) {
     return units[dev][cl];
 }
 
+// CTAs of a stream-K launch: every co-resident CTA, at most kSkMaxCtas and at
+// most one per (tile, k-block) unit; 0 when the device query fails.
+template <int BN>
+int sk_ctas(int64_t units) {
+    int64_t P = resident_units<BN, false>(1);
+    if (P > kSkMaxCtas) P = kSkMaxCtas;
+    if (P > units) P = units;
+    return (int)P;
+}
+
+// Whether stream-K applies to the problem with BN-column tiles and its
+// scratch holds what the launch needs (single-CTA tiles, M <= KSPLIT_ROWS,
+// no dual B).
+template <int BN>
+bool sk_fits(const GemmProblem& pr, int64_t tiles, int64_t units) {
+    if (pr.sk_part == nullptr || pr.sk_cnt == nullptr || pr.M > KSPLIT_ROWS || pr.dual) return false;
+    if (units > 0x7fffffff || 2 * tiles > pr.sk_cnt_cap) return false;
+    const int P = sk_ctas<BN>(units);
+    const int64_t rows = 32 * ((pr.M + 31) / 32);
+    return P >= 1 && (size_t)P * 2 * rows * BN * 4 <= pr.sk_part_bytes;
+}
+
 // ks > 1: split each tile's K range across a cluster of ks CTAs (single-CTA
 // tiles, M <= KSPLIT_ROWS, no dual B; one tile per cluster).
+// ks == 0: stream-K (single-CTA tiles, M <= KSPLIT_ROWS, no dual B): the
+// tiles' k-blocks are dealt out evenly to all CTAs and tiles split between
+// CTAs are summed through the problem's scratch.
 template <int BN, bool PAIR>
 tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     using C = Cfg<BN, PAIR>;
@@ -892,10 +1070,23 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
         kp.raster = shared_a ? 1 : (shared_b ? 2 : 0);
         kp.band = GROUP_M;
     }
+    const bool sk = ks == 0;
+    if (sk) ks = 1;
     kp.ksplit = ks;
     if (ks > 1 && (PAIR || pr.dual || pr.M > KSPLIT_ROWS || ks > C::MAX_KSPLIT || ks > 8 ||
                    ks > (pr.fold ? G : 1) * kp.k_blocks))
         return TPMLP_ERR_SHAPE;
+    const int64_t sk_units = (int64_t)kp.num_tiles * (pr.fold ? G : 1) * kp.k_blocks;
+    int sk_grid = 0;
+    if (sk) {
+        if (PAIR || !sk_fits<BN>(pr, kp.num_tiles, sk_units)) return TPMLP_ERR_SHAPE;
+        sk_grid = sk_ctas<BN>(sk_units);
+        kp.sk = 1;
+        kp.sk_units = (int)sk_units;
+        kp.sk_rows = 32 * ((pr.M + 31) / 32);
+        kp.sk_part = pr.sk_part;
+        kp.sk_cnt = pr.sk_cnt;
+    }
     kp.epi = pr.epi;
     kp.err = device_error_word();
     kp.timeout_ns = wait_timeout_ns();
@@ -917,13 +1108,19 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     }
     const int max_units = resident_units<BN, PAIR>(PAIR ? 2 : 1);
     if (max_units < 1) return TPMLP_ERR_CUDA;
-    // persistent units, or one cluster per tile when K is split
-    const int units = ks > 1 ? kp.num_tiles : (kp.num_tiles < max_units ? kp.num_tiles : max_units);
+    // persistent units, one cluster per tile when K is split, or the
+    // stream-K CTAs
+    const int units = sk ? sk_grid
+                         : ks > 1 ? kp.num_tiles
+                                  : (kp.num_tiles < max_units ? kp.num_tiles : max_units);
     cfg.gridDim = dim3((unsigned)(units * cl));
     cudaError_t e;
     {
         LaunchScope ls(pr.name, s);
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, kp);
+        // the arrival counters start at zero (a memset node inside a graph)
+        e = sk ? cudaMemsetAsync(pr.sk_cnt, 0, (size_t)kp.num_tiles * 2 * sizeof(int), s)
+               : cudaSuccess;
+        if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, kp);
     }
     if (e != cudaSuccess) return TPMLP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
@@ -955,7 +1152,9 @@ Plan choose_plan(const GemmProblem& pr) {
         int ks;
         double rate;
     };
+    // ks = 0: stream-K (M <= 64, with the scratch)
     const Cand cands[] = {{256, true, 1, 1.08}, {256, false, 1, 1.0}, {128, false, 1, 0.85},
+                          {256, false, 0, 1.0},  {128, false, 0, 0.85},
                           {256, false, 2, 1.0},  {256, false, 3, 1.0}, {256, false, 4, 1.0},
                           {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85}};
     const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
@@ -974,18 +1173,38 @@ Plan choose_plan(const GemmProblem& pr) {
         const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
         const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
                               ((pr.N + n_out - 1) / n_out);
+        // M <= 64: streamed bytes in units of (tile columns x k-blocks), plus a
+        // fixed cost per CTA start (launch, TMEM, barrier set-up, pipeline
+        // fill, the K-split exchange) of about 30 k-blocks of a 128-column
+        // tile, fitted on the N = 16, D = 12288, F = 49152 forward; a
+        // persistent launch pays it once, a K-split launch once per wave.
+        // Stream-K adds a counter reset and the partial-tile sums (charged as
+        // 10 more k-blocks) and streams ceil(units / CTAs) k-blocks per CTA
+        // at 0.8 of the rate of whole tiles: the CTAs read unrelated K
+        // ranges at a time, where whole tiles started together read the same
+        // weight rows (fitted on the same forward: stream-K takes the folded
+        // row GEMM, 220 -> 205 us, and leaves the column GEMM and the
+        // grouped partial-sum GEMM, where it measured 1-10% slower).
+        const double start = 30.0 * 128.0;
+        if (c.ks == 0) {
+            const int64_t sku = tiles * kb_total;
+            const bool fits = c.bn == 128 ? sk_fits<128>(pr, tiles, sku) : sk_fits<256>(pr, tiles, sku);
+            if (!fits) continue;
+            const int64_t P = c.bn == 128 ? sk_ctas<128>(sku) : sk_ctas<256>(sku);
+            const double cost =
+                start + 10.0 * 128.0 + (double)c.bn * (double)((sku + P - 1) / P) / 0.8;
+            if (cost < best) {
+                best = cost;
+                pick = i;
+            }
+            continue;
+        }
         int64_t units = 0;
         if (c.bn == 128) units = resident_units<128, false>(c.ks);
         else if (c.pair) units = resident_units<256, true>(2);
         else units = resident_units<256, false>(c.ks);
         if (units < 1) continue;
         const int64_t waves = (tiles + units - 1) / units;
-        // M <= 64: streamed bytes in units of (tile columns x k-blocks), plus a
-        // fixed cost per CTA start (launch, TMEM, barrier set-up, pipeline
-        // fill, the K-split exchange) of about 30 k-blocks of a 128-column
-        // tile, fitted on the N = 16, D = 12288, F = 49152 forward; a
-        // persistent launch pays it once, a K-split launch once per wave
-        const double start = 30.0 * 128.0;
         const double kb_cta = (double)((kb_total + c.ks - 1) / c.ks);
         double cost;
         if (pr.M > 64)

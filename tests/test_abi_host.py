@@ -81,6 +81,30 @@ def test_workspace_bytes(lib):
     assert lib.tpmlp_workspace_bytes(0, 1, N, D, 63, 4, 0) == ctypes.c_size_t(-1).value
 
 
+def test_workspace_bytes_balanced(lib):
+    """The balanced size adds the few-token stream-K scratch (bf16, 1 <= N <= 64)
+    after the required part rounded to 256 bytes: 2 counters per 128-column
+    tile of the widest GEMM (T groups of max(F/T, D) columns), then 256 CTAs
+    x 2 slots x round_up(N, 32) rows x 256 fp32 columns."""
+    import torch
+    r256 = lambda x: (x + 255) // 256 * 256
+    bal = B.tpmlp_workspace_bytes_balanced
+    D, F, T = 1024, 8192, 4
+    for N in (1, 16, 33, 64):
+        rows = (N + 31) // 32 * 32
+        sk = r256(2 * T * ((max(F // T, D) + 127) // 128) * 4) + 256 * 2 * rows * 256 * 4
+        for op in (0, 1):
+            for mode in ("splitk", "partials"):
+                base = B.tpmlp_workspace_bytes(op, torch.bfloat16, N, D, F, T, mode)
+                assert bal(op, torch.bfloat16, N, D, F, T, mode) == r256(base) + sk
+    # no scratch for fp32, for N > 64 and for N = 0
+    for args in ((torch.float32, 16), (torch.bfloat16, 65), (torch.bfloat16, 0)):
+        for mode in ("splitk", "partials"):
+            assert bal(0, args[0], args[1], D, F, T, mode) == \
+                B.tpmlp_workspace_bytes(0, args[0], args[1], D, F, T, mode)
+    assert lib.tpmlp_workspace_bytes_balanced(0, 1, 16, D, 63, 4, 0) == ctypes.c_size_t(-1).value
+
+
 def test_shape_errors(lib):
     assert fwd(lib, F=33, T=2) == B.ERR_SHAPE             # F % T != 0 (the pages' assert)
     assert fwd(lib, T=0) == B.ERR_SHAPE
@@ -131,11 +155,12 @@ def test_vocab_ce_and_reduce_errors(lib):
 def test_gemm_plan_argument_errors(lib):
     x = ctypes.c_int(0)
     r = ctypes.byref(x)
-    assert lib.tpmlp_gemm_plan(16, 128, 64, 1, 0, 0, None, r, r) == B.ERR_ARG
-    assert lib.tpmlp_gemm_plan(0, 128, 64, 1, 0, 0, r, r, r) == B.ERR_SHAPE
-    assert lib.tpmlp_gemm_plan(16, 128, 64, 0, 0, 0, r, r, r) == B.ERR_SHAPE
-    assert lib.tpmlp_gemm_plan(16, 128, 64, 17, 1, 0, r, r, r) == B.ERR_SHAPE
-    assert lib.tpmlp_gemm_plan(1 << 31, 128, 64, 1, 0, 0, r, r, r) == B.ERR_SHAPE
+    for bal in (0, 1):
+        assert lib.tpmlp_gemm_plan(16, 128, 64, 1, 0, 0, bal, None, r, r) == B.ERR_ARG
+        assert lib.tpmlp_gemm_plan(0, 128, 64, 1, 0, 0, bal, r, r, r) == B.ERR_SHAPE
+        assert lib.tpmlp_gemm_plan(16, 128, 64, 0, 0, 0, bal, r, r, r) == B.ERR_SHAPE
+        assert lib.tpmlp_gemm_plan(16, 128, 64, 17, 1, 0, bal, r, r, r) == B.ERR_SHAPE
+        assert lib.tpmlp_gemm_plan(1 << 31, 128, 64, 1, 0, 0, bal, r, r, r) == B.ERR_SHAPE
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

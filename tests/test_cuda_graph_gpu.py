@@ -5,8 +5,9 @@ between calls that a replay would miss (tensor maps and kernel parameters are
 passed by value at launch), so a forward + backward step, or a CE forward and
 backward, captured once and replayed, must give bit-identical results to the
 same calls made eagerly: all kernels are deterministic. The shapes cover the
-CTA-pair GEMM, the K-split GEMM (a few token rows), the fp32 CUDA-core GEMM
-and both block-end modes.
+CTA-pair GEMM, the K-split GEMM (a few token rows), the stream-K GEMM (a few
+token rows with the scratch: a counter reset and a launch per GEMM, partial
+tiles summed in CTA order), the fp32 CUDA-core GEMM and both block-end modes.
 """
 
 import pytest
@@ -31,7 +32,7 @@ def dev():
     return torch.device("cuda:0")
 
 
-def block_buffers(N, D, F, T, dtype, mode, seed):
+def block_buffers(N, D, F, T, dtype, mode, seed, balanced=False):
     g = torch.Generator(device=dev())
     g.manual_seed(seed)
     Fs = F // T
@@ -47,8 +48,9 @@ def block_buffers(N, D, F, T, dtype, mode, seed):
         "dW1": [torch.empty(D, Fs, dtype=dtype, device=dev()) for _ in range(T)],
         "dW2": [torch.empty(Fs, D, dtype=dtype, device=dev()) for _ in range(T)],
     }
-    wf = tp.tpmlp_workspace_bytes(_binding.OP_FORWARD, dtype, N, D, F, T, mode)
-    wb = tp.tpmlp_workspace_bytes(_binding.OP_BACKWARD, dtype, N, D, F, T, mode)
+    size = tp.tpmlp_workspace_bytes_balanced if balanced else tp.tpmlp_workspace_bytes
+    wf = size(_binding.OP_FORWARD, dtype, N, D, F, T, mode)
+    wb = size(_binding.OP_BACKWARD, dtype, N, D, F, T, mode)
     b["ws"] = torch.empty(max(wf, wb, 256), dtype=torch.uint8, device=dev())
     return b
 
@@ -64,14 +66,16 @@ def outputs(b):
     return [t.clone() for t in [b["Y"], b["dX"], *b["H"], *b["dW1"], *b["dW2"]]]
 
 
-@pytest.mark.parametrize("N,D,F,T,dtype,mode", [
-    (512, 512, 2048, 2, torch.bfloat16, "splitk"),      # CTA-pair tiles
-    (16, 1024, 8192, 4, torch.bfloat16, "splitk"),      # K-split row and dX GEMMs
-    (16, 1024, 8192, 4, torch.bfloat16, "partials"),    # partial sums + block-end reduce
-    (64, 256, 1024, 2, torch.float32, "splitk"),        # fp32 CUDA-core GEMM
+@pytest.mark.parametrize("N,D,F,T,dtype,mode,balanced", [
+    (512, 512, 2048, 2, torch.bfloat16, "splitk", False),      # CTA-pair tiles
+    (16, 1024, 8192, 4, torch.bfloat16, "splitk", False),      # K-split row and dX GEMMs
+    (16, 1024, 8192, 4, torch.bfloat16, "partials", False),    # partial sums + block-end reduce
+    (16, 1024, 8192, 4, torch.bfloat16, "splitk", True),       # stream-K GEMMs
+    (40, 2048, 8000, 4, torch.bfloat16, "partials", True),     # stream-K, 64-row slots
+    (64, 256, 1024, 2, torch.float32, "splitk", False),        # fp32 CUDA-core GEMM
 ])
-def test_graph_replay_matches_eager_bit_for_bit(N, D, F, T, dtype, mode):
-    b = block_buffers(N, D, F, T, dtype, mode, seed=N + D + T)
+def test_graph_replay_matches_eager_bit_for_bit(N, D, F, T, dtype, mode, balanced):
+    b = block_buffers(N, D, F, T, dtype, mode, seed=N + D + T, balanced=balanced)
     step(b, mode)                     # eager (also loads modules, sets kernel attributes)
     torch.cuda.synchronize()
     want = outputs(b)

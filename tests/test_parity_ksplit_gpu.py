@@ -69,8 +69,14 @@ def run_block(rows, D, mode, seed):
     gW1 = [W1[:, r * FS:(r + 1) * FS].contiguous().to(dev()) for r in range(T)]
     gW2 = [W2[r * FS:(r + 1) * FS].contiguous().to(dev()) for r in range(T)]
     gX = X.to(dev())
-    Y, H, Z = tp.mlp_forward(gX, gW1, gW2, act="gelu_tanh", mode=mode)
-    dX, dW1, dW2, _, _ = tp.mlp_backward(gX, gW1, gW2, H, Z, dY.to(dev()), act="gelu_tanh", mode=mode)
+    # workspaces of the required size only: without the stream-K scratch the
+    # few-token GEMMs take the cluster split that the plan above reports
+    F = T * FS
+    ws = [torch.empty(max(tp.tpmlp_workspace_bytes(op, torch.bfloat16, rows, D, F, T, mode), 256),
+                      dtype=torch.uint8, device=dev()) for op in (0, 1)]
+    Y, H, Z = tp.mlp_forward(gX, gW1, gW2, act="gelu_tanh", mode=mode, workspace=ws[0])
+    dX, dW1, dW2, _, _ = tp.mlp_backward(gX, gW1, gW2, H, Z, dY.to(dev()), act="gelu_tanh", mode=mode,
+                                         workspace=ws[1])
     torch.cuda.synchronize()
     f = oracle.mlp.forward(X, W1, None, W2, None, "gelu_tanh")
     b = oracle.mlp.backward(X, W1, None, W2, dY, "gelu_tanh")
