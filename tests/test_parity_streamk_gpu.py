@@ -44,11 +44,9 @@ def col_plan(N, D, T, balanced=True):
 
 def test_plans_take_stream_k_only_with_the_scratch_and_few_rows():
     # the weight-streaming forward of N=16, D=12288, F=49152, T=8: the folded
-    # row GEMM (96 tiles for 152 SMs) takes stream-K; the column GEMM (384
-    # tiles, started together on the same weight rows) keeps whole tiles
+    # row GEMM (96 tiles for 152 SMs) takes stream-K
     assert tp.tpmlp_gemm_plan(16, 12288, 6144, 8, fold=True, balanced=True)[2] == 0
     assert tp.tpmlp_gemm_plan(16, 12288, 6144, 8, fold=True, balanced=False)[2] != 0
-    assert tp.tpmlp_gemm_plan(16, 6144, 12288, 8, balanced=True) == (128, 1, 1)
     # a few tiles of a small block take it (the shapes below)
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=True)[2] == 0
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=False)[2] != 0
@@ -69,9 +67,9 @@ def shapes():
     return out
 
 
-def inputs(N, D, T, seed):
+def inputs(N, D, T, seed, fs=FS):
     g = torch.Generator().manual_seed(seed)
-    F = T * FS
+    F = T * fs
     X = torch.randn(N, D, generator=g).to(torch.bfloat16)
     W1 = (torch.randn(D, F, generator=g) / D ** 0.5).to(torch.bfloat16)
     W2 = (torch.randn(F, D, generator=g) / F ** 0.5).to(torch.bfloat16)
@@ -84,9 +82,10 @@ def inputs(N, D, T, seed):
 def run(X, W1, W2, b1, b2, dY, T, mode, balanced):
     N, D = X.shape
     F = W1.shape[1]
-    gW1 = [W1[:, r * FS:(r + 1) * FS].contiguous().to(dev()) for r in range(T)]
-    gW2 = [W2[r * FS:(r + 1) * FS].contiguous().to(dev()) for r in range(T)]
-    gb1 = [b1[r * FS:(r + 1) * FS].contiguous().to(dev()) for r in range(T)]
+    fs = F // T
+    gW1 = [W1[:, r * fs:(r + 1) * fs].contiguous().to(dev()) for r in range(T)]
+    gW2 = [W2[r * fs:(r + 1) * fs].contiguous().to(dev()) for r in range(T)]
+    gb1 = [b1[r * fs:(r + 1) * fs].contiguous().to(dev()) for r in range(T)]
     size = tp.tpmlp_workspace_bytes_balanced if balanced else tp.tpmlp_workspace_bytes
     wsf = torch.empty(max(size(_binding.OP_FORWARD, X.dtype, N, D, F, T, mode), 256),
                       dtype=torch.uint8, device=dev())
@@ -119,6 +118,26 @@ def test_stream_k_forward_backward_against_oracle(mode):
         assert_close(dX, b["dX"], "bf16", "dX " + tag)
         assert_close(dW1, b["dW1"], "bf16", "dW1 " + tag)
         assert_close(dW2, b["dW2"], "bf16", "dW2 " + tag)
+
+
+@pytest.mark.parametrize("mode", ["splitk", "partials"])
+def test_stream_k_with_more_tiles_than_sms(mode):
+    """8 x 21 = 168 column tiles for 152 SMs: most CTAs' ranges end inside
+    one tile and start inside the next, so both scratch slots of a CTA are
+    in use. F/T = 2600 ends every shard in a ragged k-block and a ragged
+    tile."""
+    N, D, T, fs = 16, 4096, 8, 2600
+    bn, _, ks = tp.tpmlp_gemm_plan(N, fs, D, T, balanced=True)
+    assert ks == 0 and T * -(-fs // bn) > 152, (bn, ks)
+    X, W1, W2, b1, b2, dY = inputs(N, D, T, seed=99, fs=fs)
+    Y, H, dX, dW1, dW2 = run(X, W1, W2, b1, b2, dY, T, mode, balanced=True)
+    f = oracle.mlp.forward(X, W1, b1, W2, b2, "gelu_tanh")
+    b = oracle.mlp.backward(X, W1, b1, W2, dY, "gelu_tanh")
+    assert_close(Y, f["Y"], "bf16", "Y")
+    assert_close(H, f["H"], "bf16", "H")
+    assert_close(dX, b["dX"], "bf16", "dX")
+    assert_close(dW1, b["dW1"], "bf16", "dW1")
+    assert_close(dW2, b["dW2"], "bf16", "dW2")
 
 
 def test_stream_k_is_deterministic_and_agrees_with_the_unbalanced_form():
