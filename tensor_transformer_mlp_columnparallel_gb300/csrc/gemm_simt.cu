@@ -1,16 +1,22 @@
 // fp32 grouped / shard-folded GEMM on CUDA cores: the exact-fp32 mode of the
 // block (fmaf in fp32, no TF32 tensor cores, whose 10-bit mantissa would not
 // meet a 1e-5 relative bound). 64 x 64 output tile per CTA, 256 threads,
-// 4 x 4 outputs per thread, K staged through shared memory 16 at a time with
+// 4 x 4 outputs per thread, K staged through shared memory 32 at a time with
 // the next chunk's loads in flight in registers.
+// When the tiles are fewer than the SMs (the small blocks this mode is for),
+// a cluster of up to 8 CTAs shares one tile's K chunks; the leader adds the
+// peers' partial tiles from their shared memory in rank order (so the result
+// does not depend on timing) and runs the epilogue.
 // Same problem description and epilogue semantics as the tensor-core GEMM.
 #include "act.cuh"
+#include "ptx.cuh"
 #include "tpmlp_internal.h"
 
 namespace tpmlp {
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 16;
+constexpr int TM = 64, TN = 64, TK = 32;
+constexpr int MAX_KS = 8;   // CTAs of a K-split cluster (the portable cluster limit)
 
 struct SimtParams {
     const float* A[kMaxG];
@@ -18,6 +24,7 @@ struct SimtParams {
     const float* B2[kMaxG];   // DUAL: the up projection
     int64_t lda, ldb;
     int M, N, K, G, fold;
+    int ks;   // CTAs per tile (a cluster along z) sharing its K chunks
     EpiArgs epi;
 };
 
@@ -47,11 +54,17 @@ __device__ __forceinline__ void epi_swiglu_scalar(const EpiArgs& e, int g, int m
 
 template <bool A_MN, bool B_MN, bool DUAL>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
-    __shared__ float As[TK][TM + 4];
-    __shared__ float Bs[TK][TN + 4];
+    // A and B stages; after the K loop the first 16 KB hold this CTA's
+    // partial tile for a K split
+    __shared__ __align__(16) float stage[2 * TK * (TM + 4)];
     __shared__ float Bs2[DUAL ? TK : 1][TN + 4];
+    float (*As)[TM + 4] = reinterpret_cast<float (*)[TM + 4]>(stage);
+    float (*Bs)[TN + 4] = reinterpret_cast<float (*)[TN + 4]>(stage + TK * (TM + 4));
+    static_assert(2 * TK * (TM + 4) >= TM * TN, "partial tile fits in the stages");
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int n0 = blockIdx.x * TN, m0 = blockIdx.y * TM;
+    const int kr = (int)blockIdx.z % p.ks;    // rank in the K-split cluster
+    const int gz = (int)blockIdx.z / p.ks;    // group (non-folded)
     float acc[4][4], acc2[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -64,13 +77,16 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
     const int ngroups = p.fold ? p.G : 1;
     const int kchunks = (p.K + TK - 1) / TK;
     const int nchunks = ngroups * kchunks;
+    // this CTA's chunks [c_lo, c_hi) (all of them unless K is split)
+    const int c_lo = (int)((int64_t)nchunks * kr / p.ks);
+    const int c_hi = (int)((int64_t)nchunks * (kr + 1) / p.ks);
     constexpr int PER = TM * TK / 256;   // A (and B) elements each thread stages
     static_assert(TM * TK == 256 * PER && TN * TK == 256 * PER, "staging split");
     float ra[PER], rb[PER], rb2[PER];
     auto fetch = [&](int c) {
         const int gi = c / kchunks;
         const int k0 = (c - gi * kchunks) * TK;
-        const int g = p.fold ? gi : (int)blockIdx.z;
+        const int g = p.fold ? gi : gz;
         const float* A = p.A[g];
         const float* B = p.B[g];
         const float* B2 = p.B2[g];
@@ -102,11 +118,13 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
             if (DUAL) Bs2[kb][nn] = rb2[u];
         }
     };
-    fetch(0);
-    stash();
+    if (c_lo < c_hi) {
+        fetch(c_lo);
+        stash();
+    }
     __syncthreads();
-    for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks) fetch(c + 1);
+    for (int c = c_lo; c < c_hi; ++c) {
+        if (c + 1 < c_hi) fetch(c + 1);
 #pragma unroll
         for (int kk = 0; kk < TK; ++kk) {
             float a[4], b[4];
@@ -129,12 +147,39 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
             }
         }
         __syncthreads();
-        if (c + 1 < nchunks) {
+        if (c + 1 < c_hi) {
             stash();
             __syncthreads();
         }
     }
-    const int g_out = p.fold ? 0 : (int)blockIdx.z;
+    if (!DUAL && p.ks > 1) {
+        // peers publish their partial tile in their own shared memory; the
+        // leader adds them in rank order; every CTA stays until the leader
+        // has read it
+        float4* red = reinterpret_cast<float4*>(stage);
+        if (kr != 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                red[i * 256 + threadIdx.x] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
+        cluster_sync();
+        if (kr == 0) {
+            for (int r = 1; r < p.ks; ++r) {
+                const uint32_t peer = mapa_shared(smem_u32(red), (uint32_t)r);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = ld_cluster_v4(peer + (uint32_t)(i * 256 + threadIdx.x) * 16u);
+                    acc[i][0] += v.x;
+                    acc[i][1] += v.y;
+                    acc[i][2] += v.z;
+                    acc[i][3] += v.w;
+                }
+            }
+        }
+        cluster_sync();
+        if (kr != 0) return;
+    }
+    const int g_out = p.fold ? 0 : gz;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int m = m0 + ty + 16 * i;
@@ -172,22 +217,50 @@ tpmlp_status run_gemm_simt(const GemmProblem& pr, cudaStream_t s) {
     kp.epi = pr.epi;
     const unsigned gy = (unsigned)((pr.M + TM - 1) / TM);
     if (gy > 65535u) return TPMLP_ERR_SHAPE;
-    dim3 grid((pr.N + TN - 1) / TN, gy, pr.fold ? 1 : pr.G);
+    const int64_t gx = (pr.N + TN - 1) / TN;
+    const int gz = pr.fold ? 1 : pr.G;
+    // K split: as many CTAs per tile as fill the SMs once, at most MAX_KS and
+    // at most one per K chunk
+    int ks = 1;
+    if (!pr.dual) {
+        const int64_t ctas = gx * (int64_t)gy * gz;
+        const int64_t nchunks = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + TK - 1) / TK);
+        int64_t k = device_sm_count() / (ctas > 0 ? ctas : 1);
+        if (k > MAX_KS) k = MAX_KS;
+        if (k > nchunks) k = nchunks;
+        ks = k > 1 ? (int)k : 1;
+    }
+    kp.ks = ks;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)gx, gy, (unsigned)(gz * ks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    if (ks > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)ks;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e;
     {
         LaunchScope ls(pr.name, s);
         if (pr.dual) {
             if (pr.a_mn || !pr.b_mn || pr.fold) return TPMLP_ERR_ARG;   // the gated MLP's column GEMM only
-            simt_gemm_kernel<false, true, true><<<grid, 256, 0, s>>>(kp);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<false, true, true>, kp);
         } else if (pr.a_mn && pr.b_mn) {
-            simt_gemm_kernel<true, true, false><<<grid, 256, 0, s>>>(kp);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<true, true, false>, kp);
         } else if (pr.a_mn) {
-            simt_gemm_kernel<true, false, false><<<grid, 256, 0, s>>>(kp);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<true, false, false>, kp);
         } else if (pr.b_mn) {
-            simt_gemm_kernel<false, true, false><<<grid, 256, 0, s>>>(kp);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<false, true, false>, kp);
         } else {
-            simt_gemm_kernel<false, false, false><<<grid, 256, 0, s>>>(kp);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<false, false, false>, kp);
         }
     }
+    if (e != cudaSuccess) return TPMLP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }
 
