@@ -16,6 +16,17 @@ namespace tpmlp {
 namespace {
 
 constexpr int TM = 64, TN = 64, TK = 32;
+
+// 16-byte load from another CTA's shared memory (a shared::cluster address
+// from mapa_shared).
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
 constexpr int MAX_KS = 8;   // CTAs of a K-split cluster (the portable cluster limit)
 
 struct SimtParams {

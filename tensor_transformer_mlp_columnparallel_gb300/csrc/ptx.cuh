@@ -116,16 +116,6 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
-// 16-byte load from another CTA's shared memory (a shared::cluster address).
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
