@@ -176,14 +176,27 @@ size_t dz_bytes(tpmlp_dtype dt, int64_t N, int64_t Fs, int T) {
 // Optional scratch of the few-token (N <= 64) bf16 GEMMs' stream-K form: two
 // arrival counters per tile for the most tiles any GEMM of the block has
 // (T groups of up to max(F/T, D) columns in 128-column tiles), then the
-// partial-accumulator slots.
+// partial-accumulator slots of as many CTAs as the GEMMs have (tile,
+// k-block) units, at most kSkMaxCtas. Every GEMM with M = N of the block
+// has T x (N-columns / 128 tiles) x (K / 64 k-blocks) units with
+// {N-columns, K} = {F/T, D}, folded or grouped alike.
+size_t sk_part_bytes_for(int64_t M, int64_t units) {
+    const int64_t rows = M < 64 ? ((M + 31) / 32) * 32 : 64;
+    const int64_t ctas = units < kSkMaxCtas ? units : kSkMaxCtas;
+    return (size_t)ctas * 2 * (size_t)rows * kSkMaxBn * 4;
+}
 size_t sk_cnt_bytes(int64_t D, int64_t Fs, int T) {
     const int64_t cols = Fs > D ? Fs : D;
     return round256((size_t)2 * T * ((cols + 127) / 128) * sizeof(int));
 }
+int64_t sk_units_bound(int64_t D, int64_t Fs, int T) {
+    const int64_t a = ((Fs + 127) / 128) * ((D + 63) / 64);
+    const int64_t b = ((D + 127) / 128) * ((Fs + 63) / 64);
+    return (int64_t)T * (a > b ? a : b);
+}
 size_t sk_bytes(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T) {
     if (dt != TPMLP_BF16 || N < 1 || N > 64) return 0;
-    return sk_cnt_bytes(D, F / T, T) + sk_part_bytes_for(N);
+    return sk_cnt_bytes(D, F / T, T) + sk_part_bytes_for(N, sk_units_bound(D, F / T, T));
 }
 
 struct SkArea {
@@ -642,7 +655,7 @@ tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, i
         static float part_dummy;
         static int cnt_dummy;
         p.sk_part = &part_dummy;
-        p.sk_part_bytes = sk_part_bytes_for(M);
+        p.sk_part_bytes = sk_part_bytes_for(M, kSkMaxCtas);
         p.sk_cnt = &cnt_dummy;
         p.sk_cnt_cap = (int64_t)2 * G * ((N + 127) / 128);
     }

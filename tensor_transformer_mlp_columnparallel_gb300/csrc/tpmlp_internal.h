@@ -66,14 +66,10 @@ struct GemmProblem {
 };
 
 // Stream-K scratch: at most this many CTAs share the (tile, k-block) units,
-// each with two slots of up to 64 rows x 256 fp32 accumulators, and two
+// each with two slots of up to 64 rows x kSkMaxBn fp32 accumulators, and two
 // counters per tile (one per 32-row warp).
 constexpr int kSkMaxCtas = 256;
 constexpr int kSkMaxBn = 256;
-inline size_t sk_part_bytes_for(int64_t M) {
-    const int64_t rows = M < 64 ? ((M + 31) / 32) * 32 : 64;
-    return (size_t)kSkMaxCtas * 2 * (size_t)rows * kSkMaxBn * 4;
-}
 
 // bf16 inputs on tcgen05 tensor cores (TMA + mbarrier pipeline + TMEM).
 tpmlp_status run_gemm_tc(const GemmProblem& p, cudaStream_t s);
