@@ -13,14 +13,18 @@
 // Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap
 // the main loop of tile i + 1.
 //
-// Three launch forms, chosen per GEMM by run_gemm_tc:
+// Four launch forms, chosen per GEMM by run_gemm_tc:
 //   - CTA pair (cluster of 2, M > 128): cta_group::2 MMAs of M = 256; each
 //     CTA stages its own 128 A rows and half of the B rows;
 //   - single CTA, 128 x 256 or 128 x 128 tiles;
 //   - K split (folded GEMMs with M <= 64): a cluster of 2-4 CTAs shares one
 //     tile's k-blocks; the peers send their partial accumulator rows to the
 //     leader's freed stage memory over DSMEM and the leader adds them before
-//     its epilogue (one tile per cluster).
+//     its epilogue (one tile per cluster);
+//   - stream-K (M <= 64, given scratch in the caller's workspace): every CTA
+//     takes an equal contiguous share of the (tile, k-block) units; tiles
+//     shared by several CTAs are summed through the scratch by the last
+//     warp to count in, in CTA order.
 //
 // The problem is a batch of G same-shape GEMMs (one per shard r: the column
 // GEMM X W1^(r), the row GEMM H^(r) W2^(r), and the backward products) or,
