@@ -1142,14 +1142,20 @@ struct Plan {
 };
 
 Plan choose_plan(const GemmProblem& pr) {
-    // Tile choice by estimated time = waves x per-tile cost. A wave is one
-    // tile per CTA (single), per CTA pair, or per K-split cluster; the
-    // per-tile cost is its MMA work over the relative rate measured for the
-    // tile shape, or, for a few rows (M <= 64: weight streaming, HBM-bound),
-    // the operand bytes each CTA streams plus a fixed start cost.
-    // K-split candidates (folded GEMMs, M <= 64, weight streaming): a cluster
-    // of ks CTAs shares one tile's K range, so each streams 1/ks of the tile's
-    // bytes and more SMs stream when the tiles are fewer than the SMs.
+    // Tile choice by estimated time.
+    // M > 64 (tensor-bound): waves x per-tile MMA work over the relative rate
+    // measured for the tile shape; a wave is one tile per CTA or CTA pair.
+    // M <= 64 (weight streaming, HBM-bound): a wave of n CTAs that each
+    // stream b weight bytes takes max(n b / kHbm, b / r_cta): together they
+    // cannot beat HBM, and one CTA cannot stream faster than r_cta, so a
+    // wave of few CTAs leaves HBM idle (fitted on the N = 16, D = 12288,
+    // F = 24576 and 49152, T = 8 forward; every GEMM there within 6% of it).
+    // Candidates: whole tiles on persistent CTAs; for folded GEMMs a K split
+    // across a cluster of ks CTAs (one tile per cluster, a start per wave:
+    // on grouped GEMMs, which have T times the tiles, it measured slower);
+    // with the scratch, stream-K, whose CTAs read unrelated K ranges and
+    // reach kSkEff of the HBM rate of whole tiles started together on the
+    // same weight rows.
     struct Cand {
         int bn;
         bool pair;
@@ -1164,59 +1170,56 @@ Plan choose_plan(const GemmProblem& pr) {
     const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
     const int groups = pr.fold ? 1 : pr.G;
     const int64_t kb_total = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + BKB - 1) / BKB);
+    constexpr double kHbm = 6.6e12;     // B/s
+    constexpr double kSkEff = 0.87;
+    constexpr double kStart = 5e-6;     // s: launch, set-up and pipeline fill
+    constexpr double kSkFix = 2e-6;     // s: counter reset and partial-tile sums
     double best = 1e300;
     int pick = 1;
     for (int i = 0; i < ncand; ++i) {
         const Cand& c = cands[i];
         if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
-        // K split only for the folded GEMMs (the split-K shard sum): folding
-        // leaves N / BN tiles, where a grouped GEMM has T times as many; on the
-        // grouped ones a split measured slower or equal on every decode shape
         if (c.ks > 1 && (!pr.fold || pr.M > KSPLIT_ROWS || pr.dual || c.ks > kb_total)) continue;
         const int64_t tile_m = c.pair ? 256 : 128;
         const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
         const int64_t tiles = (int64_t)groups * ((pr.M + tile_m - 1) / tile_m) *
                               ((pr.N + n_out - 1) / n_out);
-        // M <= 64: streamed bytes in units of (tile columns x k-blocks), plus a
-        // fixed cost per CTA start (launch, TMEM, barrier set-up, pipeline
-        // fill, the K-split exchange) of about 30 k-blocks of a 128-column
-        // tile, fitted on the N = 16, D = 12288, F = 49152 forward; a
-        // persistent launch pays it once, a K-split launch once per wave.
-        // Stream-K adds a counter reset and the partial-tile sums (charged as
-        // 10 more k-blocks) and streams ceil(units / CTAs) k-blocks per CTA
-        // at 0.8 of the rate of whole tiles: the CTAs read unrelated K
-        // ranges at a time, where whole tiles started together read the same
-        // weight rows (fitted on the same forward: stream-K takes the folded
-        // row GEMM, 220 -> 205 us, and leaves the column GEMM and the
-        // grouped partial-sum GEMM, where it measured 1-10% slower).
-        const double start = 30.0 * 128.0;
+        // one CTA's streaming rate with BN-column tiles, and the weight bytes
+        // of a tile (all its k-blocks of BN columns, both halves if dual)
+        const double r_cta = c.bn == 128 ? 54e9 : 66e9;
+        const double tile_bytes = (double)c.bn * (double)kb_total * BKB * 2.0;
+        auto wave = [&](double ctas, double bytes) {
+            const double hbm = ctas * bytes / kHbm, one = bytes / r_cta;
+            return hbm > one ? hbm : one;
+        };
+        double cost;
         if (c.ks == 0) {
+            if (pr.M > KSPLIT_ROWS) continue;
             const int64_t sku = tiles * kb_total;
             const bool fits = c.bn == 128 ? sk_fits<128>(pr, tiles, sku) : sk_fits<256>(pr, tiles, sku);
             if (!fits) continue;
             const int64_t P = c.bn == 128 ? sk_ctas<128>(sku) : sk_ctas<256>(sku);
-            const double cost =
-                start + 10.0 * 128.0 + (double)c.bn * (double)((sku + P - 1) / P) / 0.8;
-            if (cost < best) {
-                best = cost;
-                pick = i;
+            const double b = (double)((sku + P - 1) / P) * c.bn * BKB * 2.0;
+            const double hbm = (double)P * b / (kHbm * kSkEff), one = b / r_cta;
+            cost = kStart + kSkFix + (hbm > one ? hbm : one);
+        } else {
+            int64_t units = 0;
+            if (c.bn == 128) units = resident_units<128, false>(c.ks);
+            else if (c.pair) units = resident_units<256, true>(2);
+            else units = resident_units<256, false>(c.ks);
+            if (units < 1) continue;
+            const int64_t full = tiles / units, rem = tiles % units;
+            if (pr.M > 64) {
+                cost = (double)(full + (rem ? 1 : 0)) * 128.0 * c.bn / c.rate;
+            } else if (c.ks == 1) {
+                cost = kStart + (double)full * wave((double)units, tile_bytes) +
+                       (rem ? wave((double)rem, tile_bytes) : 0.0);
+            } else {
+                const double per_cta = tile_bytes / c.ks;
+                cost = (double)full * (kStart + wave((double)(units * c.ks), per_cta)) +
+                       (rem ? kStart + wave((double)(rem * c.ks), per_cta) : 0.0);
             }
-            continue;
         }
-        int64_t units = 0;
-        if (c.bn == 128) units = resident_units<128, false>(c.ks);
-        else if (c.pair) units = resident_units<256, true>(2);
-        else units = resident_units<256, false>(c.ks);
-        if (units < 1) continue;
-        const int64_t waves = (tiles + units - 1) / units;
-        const double kb_cta = (double)((kb_total + c.ks - 1) / c.ks);
-        double cost;
-        if (pr.M > 64)
-            cost = (double)waves * 128.0 * c.bn / c.rate;
-        else if (c.ks == 1)
-            cost = start + (double)waves * c.bn * kb_cta;
-        else
-            cost = (double)waves * (start + c.bn * kb_cta);
         if (cost < best) {
             best = cost;
             pick = i;
