@@ -36,6 +36,9 @@
  * - Output buffers must not overlap input buffers, each other or the
  *   workspace (the one exception is tpmlp_vocab_ce_backward, which may run in
  *   place); overlapping buffers give undefined results.
+ * - A workspace serves one call at a time: calls whose GPU work can overlap
+ *   (other streams, other host threads without ordering) need separate
+ *   workspaces; calls on one stream may share one.
  * - bf16 path alignment: every pointer 16-byte aligned and D % 8 == 0,
  *   (F/T) % 8 == 0 (tensor-memory-access row pitches are multiples of 16
  *   bytes); otherwise TPMLP_ERR_ALIGN.
