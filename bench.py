@@ -10,12 +10,23 @@ Workload: N = 8192 tokens (B=4, L=2048), D = 8192, F = 28672, T = 8, bf16
 storage, fp32 accumulation, no bias, seeded synthetic inputs (X, dY ~ N(0,1),
 W ~ N(0, 0.02)).
 
-The JSON line also carries: the dominant kernel's roofline (CUDA-event
-durations measured live during the timed region), the float64 CPU oracle timed
-on a bounded sample of the same workload, an end-to-end number through the
-public API with host buffers, SM clocks sampled during the timed region, and
-secondary measurements (the PARTIALS variant with its block-end reduce
-kernel, and the vocab-parallel cross-entropy kernel).
+stdout gets ONE JSON line: the headline step (value over the K timed steps,
+the median of the per-step CUDA-event times, the dominant kernel's roofline
+from CUDA events recorded on its launch stream during the timed region, an
+end-to-end number through the public API with host buffers, SM clocks
+sampled during the timed region) and, as its LAST key, a compact `configs`
+map with every named workload (the exact-fp32 block, the D=4096 forward in
+both block-end modes with its reduce, the fwd+bwd step in PARTIALS mode with
+its two reduces, the weight-streaming forward in both modes, the
+vocab-parallel cross-entropy forward and backward, the reduce-scatter, the
+embedding and the gated block), each with its fraction of the peak it is
+held to and the float64 CPU oracle timed on a bounded sample of the same
+workload. Per-kernel tables go to stderr.
+
+Peaks (MEASURED_PEAKS.json): a tensor-bound number timed in a region under
+2 s is held to the burst cuBLAS bf16 rate, a longer one to the sustained
+rate; HBM-bound numbers to the measured copy bandwidth. `frac_of_nominal`
+adds the datasheet figures (2.25 PFLOP/s dense bf16, 7.9 TB/s) for context.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -36,20 +47,22 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from workloads.configs import MLP_CONFIGS, CE_CONFIGS  # noqa: E402
-from workloads.gen import gen_mlp_inputs  # noqa: E402
+from workloads.gen import gen_mlp_inputs, gen_ce_inputs  # noqa: E402
 
 WORKLOAD = "mlp_bf16_gelu_n8192_d8192_f28672_t8_fwdbwd"
 METRIC = "sharded-MLP fwd+bwd TFLOP/s (% BF16 peak); reduce & CE HBM GB/s (% peak)"
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+# datasheet figures for GB300, context only (the fractions use the measured peaks)
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0,
+           "source": "GB300 datasheet: 2.25 PFLOP/s dense bf16, HBM3e 7.9 TB/s"}
+BURST_REGION_S = 2.0   # timed regions shorter than this are held to the burst bf16 peak
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    # defaults time the power-capped steady state: a 20-step timed region after
-    # 3 warm-ups read about 2.5% higher than 100 steps after 20
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["splitk", "partials"], default="splitk")
     ap.add_argument("--no-secondary", action="store_true")
@@ -62,7 +75,9 @@ def parse():
     ap.add_argument("--only-ce", type=int, default=0, metavar="TOKENS",
                     help="time only the vocab CE forward and backward (V=128000, T=8) on TOKENS "
                          "tokens (small cases for profiling)")
-    return ap.parse_args()
+    ap.add_argument("--only-decode", action="store_true",
+                    help="time only the weight-streaming forward (N=16 D=12288 F=49152 T=8)")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -81,6 +96,14 @@ def peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def tensor_peak(pk, region_s):
+    """(peak TFLOP/s, its label) for a tensor-bound number whose timed
+    region lasted region_s seconds."""
+    if region_s >= BURST_REGION_S:
+        return pk["bf16_tflops_sustained"], f"bf16_tflops_sustained ({pk['source']})"
+    return pk["bf16_tflops"], f"bf16_tflops burst ({pk['source']})"
 
 
 class ClockSampler:
@@ -175,18 +198,18 @@ class Block:
             self.dX = e(N, D)
             self.dW1 = [e(D, Fs) for _ in range(T)]
             self.dW2 = [e(Fs, D) for _ in range(T)]
-        # the balanced size also holds the few-token GEMMs' stream-K scratch
-        wf = tp.tpmlp_workspace_bytes_balanced(0, dt, N, D, cfg.F, T, mode)
-        wb = tp.tpmlp_workspace_bytes_balanced(1, dt, N, D, cfg.F, T, mode) if with_dy else 0
-        self.ws = torch.empty(max(wf, wb, 256), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        self.set_mode(mode)
 
     def set_mode(self, mode):
         tp = self.tp
         cfg = self.cfg
         self.mode = mode
+        # the balanced size also holds the few-token GEMMs' stream-K scratch
         wsb = tp.tpmlp_workspace_bytes_balanced
         need = max(wsb(0, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode),
-                   wsb(1, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode), 256)
+                   wsb(1, self.X.dtype, cfg.N, cfg.D, cfg.F, cfg.T, mode) if self.dY is not None
+                   else 0, 256)
         if self.ws.numel() < need:
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.dev)
 
@@ -225,10 +248,13 @@ def max_over_ranks(x, world, dev):
     return float(t.item())
 
 
-def timed(fn, steps, warmup, world, dev, stream, reset=None):
-    """Device time (ms) of `steps` calls of fn after `warmup` untimed ones;
-    `reset` (e.g. the library's kernel-timing reset) runs between the two so
-    per-kernel tables cover the timed calls only."""
+def timed_steps(fn, steps, warmup, world, stream, reset=None):
+    """Runs `warmup` untimed calls, then `steps` timed calls bracketed by a
+    barrier and a synchronize on both sides. Returns (region_ms, per-call ms):
+    the region from one event pair around all calls, and each call's own
+    event pair, all recorded on `stream`. `reset` (e.g. the library's
+    kernel-timing reset) runs before the timed calls so per-kernel tables
+    cover them only."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -236,15 +262,19 @@ def timed(fn, steps, warmup, world, dev, stream, reset=None):
         reset()
     barrier(world)
     torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
+    for s, e in ev:
+        s.record(stream)
         fn()
+        e.record(stream)
     b.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    return a.elapsed_time(b)
+    return a.elapsed_time(b), [s.elapsed_time(e) for s, e in ev]
 
 
 def kernel_table(t, total_ms):
@@ -282,8 +312,9 @@ def kernel_source_hash(family="gemm"):
     return h.hexdigest()
 
 
-def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary
+def load_traffic(kernel, workload=None):
+    """DRAM bytes per full-size launch of `kernel` (on `workload`, when the
+    same kernel serves several) from the committed ncu summary
     (profiles/traffic.json), or None when that summary was taken on other
     sources of the kernel's family than the ones built now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -294,34 +325,211 @@ def load_traffic(kernel):
         fam = kernel_family(kernel)
         if d.get("source_hash", {}).get(fam) != kernel_source_hash(fam):
             return None
-        return d["kernels"].get(kernel, {}).get("dram_bytes_per_launch")
+        key = kernel if workload is None else f"{kernel}@{workload}"
+        rec = d["kernels"].get(key) or d["kernels"].get(kernel)
+        return None if rec is None else rec.get("dram_bytes_per_launch")
     except Exception:
         return None
 
 
-def cpu_baseline_mlp(cfg, tokens=96):
-    """Float64 oracle fwd+bwd on `tokens` rows of the same workload, all
-    host cores (numpy / OpenBLAS default threading). The per-token work of
-    fwd+bwd is 12 D F FLOP (two forward GEMM rows, four backward)."""
+def rnd(x, sig=4):
+    """x rounded to `sig` significant digits (compact JSON)."""
+    if x is None or not np.isfinite(x) or x == 0:
+        return x
+    return float(f"{x:.{sig}g}")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baselines (float64, on the host cores; bounded samples)
+# ---------------------------------------------------------------------------
+
+def _cores():
+    return len(os.sched_getaffinity(0))
+
+
+def _repeat(fn, min_s):
+    """Calls fn until at least min_s seconds have passed (at least once);
+    returns seconds per call."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_s:
+            return el / n
+
+
+def cpu_mlp_shard(cfg, backward, tokens=None):
+    """Float64 oracle on ONE shard of T (W1[:, :F/T], W2[:F/T, :]) of the
+    workload: exactly 1/T of the block's FLOPs, a narrower MLP of the same
+    definition. `tokens` limits the rows (all rows when None)."""
     import oracle
-    inp = gen_mlp_inputs(cfg, N=tokens)
-    W1 = oracle.mlp.as_f64(inp.W1)
-    W2 = oracle.mlp.as_f64(inp.W2)
+    N = cfg.N if tokens is None else tokens
+    inp = gen_mlp_inputs(cfg, N=N, with_dy=backward)
+    Fs = cfg.Fs
+    W1 = oracle.mlp.as_f64(inp.W1[:, :Fs])
+    W2 = oracle.mlp.as_f64(inp.W2[:Fs, :])
+    b1 = None if inp.b1 is None else oracle.mlp.as_f64(inp.b1[:Fs])
+    b2 = None if inp.b2 is None else oracle.mlp.as_f64(inp.b2)
+    X = oracle.mlp.as_f64(inp.X)
+    dY = oracle.mlp.as_f64(inp.dY) if backward else None
+
+    def run():
+        oracle.mlp.forward(X, W1, b1, W2, b2, cfg.act)
+        if backward:
+            oracle.mlp.backward(X, W1, b1, W2, dY, cfg.act)
+    sec = _repeat(run, 0.5)
+    flops = (12.0 if backward else 4.0) * N * cfg.D * Fs
+    return sec, flops, N
+
+
+def cpu_baselines():
+    """The float64 oracle as it stands, on the host cores (numpy; OpenBLAS
+    threads = host cores for the products, one core for elementwise work),
+    one bounded sample per workload, in the unit of its GPU number. Returns
+    the per-workload map and the headline workload's record."""
+    import oracle
+    out = {}
+    cores = _cores()
+    # exact-fp32 block: the whole forward, per call
+    c1 = MLP_CONFIGS["mlp_f32_relu_n64_d256_f1024_t2"]
+    inp = gen_mlp_inputs(c1, with_dy=True)
+    a = [oracle.mlp.as_f64(t) for t in (inp.X, inp.W1, inp.b1, inp.W2, inp.b2, inp.dY)]
+    f = _repeat(lambda: oracle.mlp.forward(a[0], a[1], a[2], a[3], a[4], "relu"), 0.5)
+    fb = _repeat(lambda: (oracle.mlp.forward(a[0], a[1], a[2], a[3], a[4], "relu"),
+                          oracle.mlp.backward(a[0], a[1], a[2], a[3], a[5], "relu")), 0.5)
+    out["c1"] = {"fwd_us": rnd(f * 1e6), "fwdbwd_us": rnd(fb * 1e6), "cores": cores,
+                 "sample": "whole workload"}
+    # D=4096 F=16384 T=4 forward: all shards, all tokens
+    c2 = MLP_CONFIGS["mlp_bf16_gelu_n4096_d4096_f16384_t4"]
+    inp = gen_mlp_inputs(c2, with_dy=False)
+    a = [oracle.mlp.as_f64(t) for t in (inp.X, inp.W1, inp.b1, inp.W2, inp.b2)]
     t0 = time.perf_counter()
-    oracle.mlp.forward(inp.X, W1, None, W2, None, cfg.act)
-    oracle.mlp.backward(inp.X, W1, None, W2, inp.dY, cfg.act)
-    dt = time.perf_counter() - t0
-    flops = 12.0 * tokens * cfg.D * cfg.F
-    cores = len(os.sched_getaffinity(0))
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} of {cfg.N} tokens, fwd+bwd, float64 numpy (OpenBLAS threads = "
-                      f"host cores), {dt:.1f} s"}
+    oracle.mlp.forward(a[0], a[1], a[2], a[3], a[4], c2.act)
+    sec = time.perf_counter() - t0
+    out["c2"] = {"value": rnd(c2.fwd_flops() / sec / 1e12), "unit": "TFLOP/s", "s": rnd(sec, 3),
+                 "cores": cores, "sample": "whole forward"}
+    del inp, a
+    # fwd+bwd workload: one shard of T at full N (1/T of the FLOPs)
+    c3 = MLP_CONFIGS[WORKLOAD]
+    headline = cpu_baseline_headline(c3)
+    sec = headline["s"]
+    out["c3"] = {"value": rnd(headline["value"]), "unit": "TFLOP/s", "s": rnd(sec, 3),
+                 "est_full_s": rnd(sec * c3.T, 3), "cores": cores,
+                 "sample": f"shard 0 of {c3.T}, all {c3.N} tokens, fwd+bwd"}
+    # weight-streaming forward: one shard of T, GB/s of that shard's algorithmic bytes
+    c4 = MLP_CONFIGS["mlp_bf16_gelu_n16_d12288_f49152_t8"]
+    sec, _, _ = cpu_mlp_shard(c4, backward=False)
+    b4 = decode_bytes(c4) / c4.T
+    out["c4"] = {"value": rnd(b4 / sec / 1e9), "unit": "GB/s", "s": rnd(sec, 3),
+                 "est_full_s": rnd(sec * c4.T, 3), "cores": cores,
+                 "sample": f"shard 0 of {c4.T}, fwd"}
+    # cross-entropy: as many 256-row chunks as fit in about 4 s (forward) and
+    # one chunk (backward), GB/s of the algorithmic bytes of those rows
+    c5 = CE_CONFIGS["vocab_ce_n8192_v128000_t8"]
+    ce = gen_ce_inputs(c5, N=4096)   # the sample stops after about 4 s, at most 4096 rows
+    rows, t0 = 0, time.perf_counter()
+    while rows < ce.N and (rows == 0 or time.perf_counter() - t0 < 4.0):
+        oracle.ce.vocab_ce(ce.logits[rows:rows + 256], ce.targets[rows:rows + 256], c5.T)
+        rows += 256
+    sec = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.ce.vocab_ce_backward(ce.logits[:256], ce.targets[:256], 1.0 / c5.N)
+    sb = time.perf_counter() - t0
+    out["c5"] = {"fwd_GB/s": rnd(rows * c5.V * 4.0 / sec / 1e9),
+                 "bwd_GB/s": rnd(256 * c5.V * 8.0 / sb / 1e9), "cores": 1,
+                 "sample": f"fwd {rows} of {c5.N} rows, bwd 256 rows"}
+    del ce
+    return out, headline
 
 
-def measure_embedding(dev, steps, pk):
+def cpu_baseline_headline(cfg):
+    """The headline's cpu_baseline: the float64 oracle's fwd+bwd on one
+    shard of T of the same workload (all tokens)."""
+    sec, flops, N = cpu_mlp_shard(cfg, backward=True)
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "s": sec,
+            "sample": f"shard 0 of {cfg.T} (1/{cfg.T} of the FLOPs), all {N} tokens, fwd+bwd, "
+                      f"float64 numpy (OpenBLAS threads = host cores), {sec:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# the named workloads on the GPU
+# ---------------------------------------------------------------------------
+
+def decode_bytes(fc):
+    """Algorithmic bytes of one weight-streaming forward: both weights and
+    biases once (bf16), X and Y, H and Z."""
+    wbytes = 2.0 * fc.D * fc.F * 2 + fc.F * 2 + fc.D * 2
+    return wbytes + 2.0 * fc.N * fc.D * 2 + 2.0 * fc.N * fc.F * 2
+
+
+def _lib_timed(tp, fn, iters, stream, warmup=3):
+    """Per-call median ms of fn, the timed region in s and the library's
+    per-kernel records over the timed calls."""
+    tp.tpmlp_timing_reset()
+    tp.tpmlp_timing_enable(True)
+    region, per = timed_steps(fn, iters, warmup, 1, stream, reset=tp.tpmlp_timing_reset)
+    tp.tpmlp_timing_enable(False)
+    return float(np.median(per)), region * 1e-3, tp.tpmlp_timing_read()
+
+
+def _kernel_ms(t, name):
+    k = t.get(name)
+    return None if k is None else k["total_ms"] / k["launches"]
+
+
+def _hbm_entry(gbs, ms, pk, kernel=None, workload=None):
+    e = {"value": rnd(gbs), "unit": "GB/s", "ms": rnd(ms), "frac": rnd(gbs / pk["hbm_gbs"], 3),
+         "frac_of_nominal": rnd(gbs / NOMINAL["hbm_gbs"], 3)}
+    if kernel is not None:
+        tr = load_traffic(kernel, workload)
+        if tr is not None:
+            e["traffic"] = rnd(tr)
+    return e
+
+
+def _tensor_entry(tflops, ms, region_s, pk):
+    peak, label = tensor_peak(pk, region_s)
+    return {"value": rnd(tflops), "unit": "TFLOP/s", "ms": rnd(ms), "frac": rnd(tflops / peak, 3),
+            "peak": "burst" if "burst" in label else "sustained",
+            "frac_of_nominal": rnd(tflops / NOMINAL["bf16_tflops"], 3)}
+
+
+def measure_ce(dev, stream, iters, pk, tokens=0):
+    import dataclasses
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+    ce = CE_CONFIGS["vocab_ce_n8192_v128000_t8"]
+    if tokens:
+        ce = dataclasses.replace(ce, N=tokens)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    logits = torch.randn((ce.N, ce.V), generator=g, device=dev) * ce.logit_std
+    targets = torch.randint(0, ce.V, (ce.N,), generator=g, device=dev)
+    loss = torch.empty(ce.N, device=dev)
+    mean = torch.empty(1, device=dev)
+    amax = torch.empty(ce.N, dtype=torch.int32, device=dev)
+    own = torch.empty(ce.N, dtype=torch.int32, device=dev)
+    fn = lambda: tp.tpmlp_vocab_ce(logits, targets, ce.T, loss, mean, amax, own)
+    _, _, t = _lib_timed(tp, fn, iters, stream)
+    ms = _kernel_ms(t, "vocab_ce_fwd")
+    fwd = _hbm_entry(ce.algorithmic_bytes() / (ms * 1e-3) / 1e9, ms, pk,
+                     None if tokens else "vocab_ce_fwd")
+    dlog = torch.empty_like(logits)
+    fnb = lambda: tp.tpmlp_vocab_ce_backward(logits, targets, ce.T, loss, 1.0 / ce.N, dlog)
+    _, _, t = _lib_timed(tp, fnb, iters, stream)
+    ms = _kernel_ms(t, "vocab_ce_bwd")
+    bwd_bytes = 8.0 * ce.N * ce.V + 12.0 * ce.N
+    bwd = _hbm_entry(bwd_bytes / (ms * 1e-3) / 1e9, ms, pk, None if tokens else "vocab_ce_bwd")
+    del logits, dlog
+    torch.cuda.empty_cache()
+    return {"fwd": fwd, "bwd": bwd}
+
+
+def measure_embedding(dev, iters, pk):
     """Vocab-parallel embedding: table 32000 x 8192 bf16 over T = 4 (the
     textbook page's row-parallel embedding), 8192 tokens; L2 flushed by a read
-    before every launch. Returns the record of the secondary measurements."""
+    before every launch, so the library's per-launch events are used."""
     import tensor_transformer_mlp_columnparallel_gb300 as tp
     Ve, He, Te, Ne = 32000, 8192, 4, 8192
     ge = torch.Generator(device=dev)
@@ -335,149 +543,97 @@ def measure_embedding(dev, steps, pk):
     # flush evicts) lands inside the timed launch
     flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     tp.tpmlp_timing_reset()
-    for i in range(3 + steps):
+    for i in range(3 + iters):
         flush.max()
         if i == 3:
             tp.tpmlp_timing_enable(True)
         tp.tpmlp_vocab_embedding(ids, shards, emb)
     torch.cuda.synchronize()
     tp.tpmlp_timing_enable(False)
-    k = tp.tpmlp_timing_read()["vocab_embedding"]
-    ms = k["total_ms"] / k["launches"]
+    ms = _kernel_ms(tp.tpmlp_timing_read(), "vocab_embedding")
     e_bytes = 2.0 * Ne * He * 2 + Ne * 8
-    gbs = e_bytes / (ms * 1e-3) / 1e9
-    return {
-        "kernel": "vocab_embedding", "ms_per_launch": ms, "GB/s": gbs,
-        "l2": "flushed before each launch by reading a 256 MB buffer",
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": e_bytes,
-                     "traffic": load_traffic("vocab_embedding")}}
+    e = _hbm_entry(e_bytes / (ms * 1e-3) / 1e9, ms, pk, "vocab_embedding")
+    e["l2"] = "read-flushed"
+    return e
 
 
-def secondary(dev, stream, steps, pk, ce_tokens=0):
-    import dataclasses
+def measure_configs(dev, stream, iters, pk, detail):
+    """Every named workload besides the headline step. Returns the compact
+    map of the JSON line; per-kernel tables go into `detail`."""
     import tensor_transformer_mlp_columnparallel_gb300 as tp
     out = {}
-    # vocab-parallel CE, N = 8192, V = 128000, T = 8: logits drawn on the device
-    ce = CE_CONFIGS["vocab_ce_n8192_v128000_t8"]
-    if ce_tokens:
-        ce = dataclasses.replace(ce, N=ce_tokens)
-    g = torch.Generator(device=dev)
-    g.manual_seed(0)
-    logits = torch.randn((ce.N, ce.V), generator=g, device=dev) * ce.logit_std
-    targets = torch.randint(0, ce.V, (ce.N,), generator=g, device=dev)
-    loss = torch.empty(ce.N, device=dev)
-    mean = torch.empty(1, device=dev)
-    amax = torch.empty(ce.N, dtype=torch.int32, device=dev)
-    own = torch.empty(ce.N, dtype=torch.int32, device=dev)
-    fn = lambda: tp.tpmlp_vocab_ce(logits, targets, ce.T, loss, mean, amax, own)
-    tp.tpmlp_timing_reset()
-    tp.tpmlp_timing_enable(True)
-    timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-    tp.tpmlp_timing_enable(False)
-    t = tp.tpmlp_timing_read()
-    k = t["vocab_ce_fwd"]
-    ms = k["total_ms"] / k["launches"]
-    gbs = ce.algorithmic_bytes() / (ms * 1e-3) / 1e9
-    out["vocab_ce_n8192_v128000_t8"] = {
-        "kernel": "vocab_ce_fwd", "ms_per_launch": ms, "GB/s": gbs,
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"],
-                     # the committed traffic is per full-size launch
-                     "traffic": None if ce_tokens else load_traffic("vocab_ce_fwd")}}
-    # backward of the same cross-entropy (mean reduction): read z, write dz
-    dlog = torch.empty_like(logits)
-    fnb = lambda: tp.tpmlp_vocab_ce_backward(logits, targets, ce.T, loss, 1.0 / ce.N, dlog)
-    tp.tpmlp_timing_reset()
-    tp.tpmlp_timing_enable(True)
-    timed(fnb, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-    tp.tpmlp_timing_enable(False)
-    t = tp.tpmlp_timing_read()
-    k = t["vocab_ce_bwd"]
-    ms = k["total_ms"] / k["launches"]
-    bwd_bytes = 8.0 * ce.N * ce.V + 12.0 * ce.N
-    gbs = bwd_bytes / (ms * 1e-3) / 1e9
-    out["vocab_ce_backward_n8192_v128000_t8"] = {
-        "kernel": "vocab_ce_bwd", "ms_per_launch": ms, "GB/s": gbs,
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"],
-                     "traffic": None if ce_tokens else load_traffic("vocab_ce_bwd"),
-                     "algorithmic_bytes_per_launch": bwd_bytes}}
-    del logits, dlog
-    torch.cuda.empty_cache()
-    if ce_tokens:
-        return out
-    # block end as a reduce-scatter (T = 8 fp32 partials of [8192, 8192] -> 8 bf16
-    # row blocks of [1024, 8192]); the partials exceed L2
-    Tn, Nn, Dn = 8, 8192, 8192
-    parts = [torch.randn(Nn, Dn, device=dev) for _ in range(Tn)]
-    rows_out = [torch.empty(Nn // Tn, Dn, dtype=torch.bfloat16, device=dev) for _ in range(Tn)]
-    b2 = torch.zeros(Dn, dtype=torch.bfloat16, device=dev)
-    fn = lambda: tp.tpmlp_block_reduce_scatter(parts, b2, rows_out)
-    tp.tpmlp_timing_reset()
-    tp.tpmlp_timing_enable(True)
-    timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-    tp.tpmlp_timing_enable(False)
-    k = tp.tpmlp_timing_read()["block_reduce_scatter_bias"]
-    ms = k["total_ms"] / k["launches"]
-    rs_bytes = Tn * Nn * Dn * 4 + Nn * Dn * 2 + Dn * 2
-    gbs = rs_bytes / (ms * 1e-3) / 1e9
-    out["block_reduce_scatter_t8_n8192_d8192"] = {
-        "kernel": "block_reduce_scatter_bias", "ms_per_launch": ms, "GB/s": gbs,
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": rs_bytes,
-                     "traffic": load_traffic("block_reduce_scatter_bias")}}
-    del parts, rows_out
-    torch.cuda.empty_cache()
-    out["vocab_embedding_v32000_h8192_t4_n8192"] = measure_embedding(dev, steps, pk)
-    torch.cuda.empty_cache()
-    # forward-only workloads: N=4096 D=4096 F=16384 T=4 (tensor-bound) and
-    # N=16 D=12288 F=49152 T=8 (weight streaming, HBM-bound)
-    for name in ("mlp_bf16_gelu_n4096_d4096_f16384_t4", "mlp_bf16_gelu_n16_d12288_f49152_t8"):
-        fc = MLP_CONFIGS[name]
-        fb = Block(fc, "splitk", dev, with_dy=False)
-        for mode in ("splitk", "partials"):
-            fb.set_mode(mode)
-            tp.tpmlp_timing_reset()
-            tp.tpmlp_timing_enable(True)
-            ms_f = timed(fb.forward, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-            tp.tpmlp_timing_enable(False)
-            t = tp.tpmlp_timing_read()
-            flops = fc.fwd_flops()
-            wbytes = 2.0 * fc.D * fc.F * 2 + fc.F * 2 + fc.D * 2      # W1, W2, b1, b2 (bf16)
-            abytes = wbytes + 2.0 * fc.N * fc.D * 2 + 2.0 * fc.N * fc.F * 2   # + X, Y, H, Z
-            rec = {"mode": mode, "ms_per_forward": ms_f / steps,
-                   "TFLOP/s": flops * steps / (ms_f * 1e-3) / 1e12,
-                   "GB/s": abytes * steps / (ms_f * 1e-3) / 1e9,
-                   "kernels": kernel_table(t, ms_f)}
-            if fc.N <= 64:
-                rec["roofline"] = {"bound": "hbm", "achieved": rec["GB/s"], "peak": pk["hbm_gbs"],
-                                   "unit": "GB/s", "frac": rec["GB/s"] / pk["hbm_gbs"],
-                                   "algorithmic_bytes_per_forward": abytes}
-            else:
-                rec["roofline"] = {"bound": "tensor", "achieved": rec["TFLOP/s"],
-                                   "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                                   "frac": rec["TFLOP/s"] / pk["bf16_tflops_sustained"]}
-            out[f"{name}_{mode}"] = rec
-        del fb
-        torch.cuda.empty_cache()
-    # the exact-fp32 block, N=64 D=256 F=1024 T=2 (ReLU, biases): latency-bound
-    # (67 MFLOP forward), so time per call, eager and replayed from a CUDA graph
+    # c1: the exact-fp32 block, N=64 D=256 F=1024 T=2 (ReLU, biases):
+    # latency-bound (67 MFLOP forward), per call eager and from a CUDA graph
     fc = MLP_CONFIGS["mlp_f32_relu_n64_d256_f1024_t2"]
     fb = Block(fc, "splitk", dev)
-    rec = {"note": "latency-bound; time reported, no roofline claim"}
-    for label, fn in (("forward", fb.forward), ("forward+backward", fb.step)):
-        ms_e = timed(fn, steps, 3, 1, dev, stream) / steps
+    rec = {}
+    for label, fn in (("fwd", fb.forward), ("fwdbwd", fb.step)):
+        ms_e, _, _ = _lib_timed(tp, fn, iters, stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for _ in range(10):
                 fn()
         graph.replay()
         torch.cuda.synchronize()
-        ms_g = timed(graph.replay, max(1, steps // 10), 1, 1, dev, stream) / (10 * max(1, steps // 10))
-        rec[label] = {"us_per_call_eager": ms_e * 1e3, "us_per_call_graph": ms_g * 1e3}
-    out["mlp_f32_relu_n64_d256_f1024_t2_latency"] = rec
+        _, per = timed_steps(graph.replay, max(3, iters // 2), 1, 1, stream)
+        rec[f"{label}_us"] = rnd(ms_e * 1e3)
+        rec[f"{label}_us_graph"] = rnd(float(np.median(per)) * 1e3 / 10)
+    out["c1 fp32 N64 D256 F1024 T2 (latency)"] = rec
     del fb
+    torch.cuda.empty_cache()
+    # c2, c4: forward-only workloads in both block-end modes
+    for key, name in (("c2 fwd N4096 D4096 F16384 T4", "mlp_bf16_gelu_n4096_d4096_f16384_t4"),
+                      ("c4 fwd N16 D12288 F49152 T8", "mlp_bf16_gelu_n16_d12288_f49152_t8")):
+        fc = MLP_CONFIGS[name]
+        fb = Block(fc, "splitk", dev, with_dy=False)
+        rec = {}
+        for mode in ("splitk", "partials"):
+            fb.set_mode(mode)
+            ms, region, t = _lib_timed(tp, fb.forward, iters, stream)
+            detail[f"{name}_{mode}"] = kernel_table(t, ms * iters)
+            if fc.N <= 64:
+                rec[mode] = _hbm_entry(decode_bytes(fc) / (ms * 1e-3) / 1e9, ms, pk)
+            else:
+                rec[mode] = _tensor_entry(fc.fwd_flops() / (ms * 1e-3) / 1e12, ms, region, pk)
+                if mode == "partials":
+                    rms = _kernel_ms(t, "block_reduce_bias")
+                    rb = fc.T * fc.N * fc.D * 4.0 + fc.N * fc.D * 2.0 + fc.D * 2.0
+                    rec["reduce"] = _hbm_entry(rb / (rms * 1e-3) / 1e9, rms, pk)
+        out[key] = rec
+        del fb
+        torch.cuda.empty_cache()
+    # c3 in PARTIALS mode: T fp32 partials + the block-end reduce for Y and dX
+    cfg = MLP_CONFIGS[WORKLOAD]
+    blk = Block(cfg, "partials", dev)
+    n3 = max(10, iters // 2)
+    ms, region, t = _lib_timed(tp, blk.step, n3, stream)
+    detail["c3_partials"] = kernel_table(t, ms * n3)
+    rec = {"partials": _tensor_entry((cfg.fwd_flops() + cfg.bwd_flops()) / (ms * 1e-3) / 1e12,
+                                     ms, region, pk)}
+    rb = cfg.T * cfg.N * cfg.D * 4.0 + cfg.N * cfg.D * 2.0
+    for name, short in (("block_reduce_bias", "reduce_y"), ("block_reduce_dx", "reduce_dx")):
+        rms = _kernel_ms(t, name)
+        rec[short] = _hbm_entry(rb / (rms * 1e-3) / 1e9, rms, pk, name)
+    out["c3 fwd+bwd N8192 D8192 F28672 T8"] = rec
+    del blk
+    torch.cuda.empty_cache()
+    # c5: vocab-parallel cross-entropy, forward and backward
+    out["c5 CE N8192 V128000 T8"] = measure_ce(dev, stream, iters, pk)
+    # block end as a reduce-scatter (T = 8 fp32 partials of [8192, 8192] -> 8 bf16
+    # row blocks of [1024, 8192]); the partials exceed L2
+    Tn, Nn, Dn = 8, 8192, 8192
+    parts = [torch.randn(Nn, Dn, device=dev) for _ in range(Tn)]
+    rows_out = [torch.empty(Nn // Tn, Dn, dtype=torch.bfloat16, device=dev) for _ in range(Tn)]
+    b2 = torch.zeros(Dn, dtype=torch.bfloat16, device=dev)
+    _, _, t = _lib_timed(tp, lambda: tp.tpmlp_block_reduce_scatter(parts, b2, rows_out), iters,
+                         stream)
+    rms = _kernel_ms(t, "block_reduce_scatter_bias")
+    rs_bytes = Tn * Nn * Dn * 4 + Nn * Dn * 2 + Dn * 2
+    out["reduce-scatter T8 N8192 D8192"] = _hbm_entry(rs_bytes / (rms * 1e-3) / 1e9, rms, pk,
+                                                      "block_reduce_scatter_bias")
+    del parts, rows_out
+    torch.cuda.empty_cache()
+    out["embedding V32000 H8192 T4 N8192"] = measure_embedding(dev, iters, pk)
     torch.cuda.empty_cache()
     # gated (SwiGLU) block, N=4096 D=4096 F=16384 T=4: gate and up as one dual
     # GEMM per shard, then the split-K down projection
@@ -492,43 +648,12 @@ def secondary(dev, stream, steps, pk, ce_tokens=0):
     Yg = torch.empty(Ns, Ds, dtype=torch.bfloat16, device=dev)
     Hg = [torch.empty(Ns, Fg // Tg, dtype=torch.bfloat16, device=dev) for _ in range(Tg)]
     fn = lambda: tp.tpmlp_swiglu_forward(Xg, Wg, Wu, Wd, Yg, Hg, None, None, "splitk", None)
-    tp.tpmlp_timing_reset()
-    tp.tpmlp_timing_enable(True)
-    ms_s = timed(fn, steps, 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-    tp.tpmlp_timing_enable(False)
-    t = tp.tpmlp_timing_read()
-    sflops = 6.0 * Ns * Ds * Fg
-    out["swiglu_bf16_n4096_d4096_f16384_t4_splitk"] = {
-        "TFLOP/s": sflops * steps / (ms_s * 1e-3) / 1e12, "ms_per_forward": ms_s / steps,
-        "kernels": kernel_table(t, ms_s),
-        "roofline": {"bound": "tensor", "achieved": sflops * steps / (ms_s * 1e-3) / 1e12,
-                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": sflops * steps / (ms_s * 1e-3) / 1e12 / pk["bf16_tflops_sustained"]}}
+    ms, region, t = _lib_timed(tp, fn, iters, stream)
+    detail["swiglu"] = kernel_table(t, ms * iters)
+    out["swiglu fwd N4096 D4096 F16384 T4"] = _tensor_entry(6.0 * Ns * Ds * Fg / (ms * 1e-3) / 1e12,
+                                                            ms, region, pk)
     del Xg, Wg, Wu, Wd, Yg, Hg
     torch.cuda.empty_cache()
-    # the PARTIALS variant of the same fwd+bwd step: T fp32 partials + block reduce
-    cfg = MLP_CONFIGS[WORKLOAD]
-    blk = Block(cfg, "partials", dev)
-    tp.tpmlp_timing_reset()
-    tp.tpmlp_timing_enable(True)
-    ms_total = timed(blk.step, max(3, steps // 2), 3, 1, dev, stream, reset=tp.tpmlp_timing_reset)
-    tp.tpmlp_timing_enable(False)
-    t = tp.tpmlp_timing_read()
-    nsteps = max(3, steps // 2)
-    flops = (cfg.fwd_flops() + cfg.bwd_flops()) * nsteps
-    red_bytes = cfg.T * cfg.N * cfg.D * 4 + cfg.N * cfg.D * 2   # read T fp32 partials, write bf16
-    rk = {}
-    for name in ("block_reduce_bias", "block_reduce_dx"):
-        if name in t:
-            ms = t[name]["total_ms"] / t[name]["launches"]
-            gbs = red_bytes / (ms * 1e-3) / 1e9
-            rk[name] = {"ms_per_launch": ms, "GB/s": gbs,
-                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
-                                     "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
-                                     "traffic": load_traffic(name)}}
-    out["partials_variant_" + WORKLOAD] = {
-        "TFLOP/s": flops / (ms_total * 1e-3) / 1e12, "ms_per_step": ms_total / nsteps,
-        "reduce_kernels": rk, "kernels": kernel_table(t, ms_total)}
     return out
 
 
@@ -634,7 +759,7 @@ def run_ours(args):
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
     launches0 = tp.tpmlp_launch_count()
-    ms = timed(blk.step, args.steps, 0, world, dev, stream)
+    ms, per_step = timed_steps(blk.step, args.steps, 0, world, stream)
     launches = tp.tpmlp_launch_count() - launches0
     tp.tpmlp_timing_enable(False)
     clk = clocks.stop()
@@ -644,23 +769,26 @@ def run_ours(args):
         raise RuntimeError(f"device error word {status} after the timed region")
 
     ms_max = max_over_ranks(ms, world, dev)
+    region_s = ms_max * 1e-3
     flops_step = cfg.fwd_flops() + cfg.bwd_flops()
-    value = flops_step * args.steps * world / (ms_max * 1e-3) / 1e12
+    value = flops_step * args.steps * world / region_s / 1e12
     ktab = kernel_table(kt, ms)
     dom = max(kt.items(), key=lambda kv: kv[1]["total_ms"])[0]
     dom_ms = kt[dom]["total_ms"] / kt[dom]["launches"]
     gemm_flops = 2.0 * cfg.N * cfg.D * cfg.F      # every GEMM of the step has this size
     achieved = gemm_flops / (dom_ms * 1e-3) / 1e12
-    peak = pk["bf16_tflops_sustained"]
+    peak, peak_label = tensor_peak(pk, region_s)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": load_traffic(dom), "kernel": dom,
-            "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a "
-                           f"back-to-back step loop)",
+            "peak_source": f"{peak_label}; timed region {region_s:.2f} s",
+            "frac_of_nominal": achieved / NOMINAL["bf16_tflops"],
+            "nominal_peak": NOMINAL["bf16_tflops"],
             "algorithmic_flops_per_launch": gemm_flops}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "ms_per_step_median": float(np.median(per_step)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; X, dY ~ N(0,1), W ~ N(0,0.02))",
         "config": {"workload": cfg.name, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
@@ -672,25 +800,36 @@ def run_ours(args):
         "roofline": roof,
         "gpu_launches": launches,
         "clocks": clk,
-        "kernels": ktab,
     }
+    detail = {"kernels_headline": ktab}
     if rank == 0 and not args.no_e2e:
         n_e = args.steps
         e_ms, h2d, d2h = e2e_measure(blk, n_e, stream)
         line["e2e"] = {"value": flops_step * n_e / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms / n_e, "steps": n_e,
-                       "copies": "batch X, dY in and results Y, dX out every step, pinned host "
-                                 "memory, overlapped with compute on two copy streams; weights and "
-                                 "their gradients resident"}
+                       "copies": "X, dY in and Y, dX out every step (pinned host memory, two copy "
+                                 "streams overlapped with compute); weights resident"}
     del blk
     torch.cuda.empty_cache()
+    configs = None
     if rank == 0 and not args.no_secondary:
-        line["secondary"] = secondary(dev, stream, args.steps, pk)
+        configs = measure_configs(dev, stream, max(20, args.steps), pk, detail)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_mlp(cfg)
+        if configs is None or args.shape:
+            line["cpu_baseline"] = cpu_baseline_headline(cfg)
+        else:
+            per_cfg, line["cpu_baseline"] = cpu_baselines()
+            for k, v in per_cfg.items():
+                for ck in configs:
+                    if ck.startswith(k + " "):
+                        configs[ck]["cpu"] = v
+        line["cpu_baseline"].pop("s", None)
     if rank == 0:
-        print(json.dumps(line))
+        sys.stderr.write("detail: " + json.dumps(detail) + "\n")
+        if configs is not None:
+            line["configs"] = configs        # last key: the end of the line is what logs keep
+        print(json.dumps(line, separators=(",", ":")))
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -721,7 +860,7 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     flops = 12.0 * tokens * cfg.D * cfg.F * args.steps
     value = flops / dt / 1e12
-    cores = len(os.sched_getaffinity(0))
+    cores = _cores()
     sample = (f"{tokens} of {cfg.N} tokens per step, fwd+bwd, float64 numpy (OpenBLAS threads = "
               f"host cores)")
     print(json.dumps({
@@ -738,31 +877,37 @@ def run_reference(args):
     }))
 
 
-def run_only_ce(args):
+def _only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()
-    out = secondary(dev, torch.cuda.current_stream(dev), args.steps, peaks(), args.only_ce)
-    print(json.dumps({"only": "vocab_ce", "tokens": args.only_ce, "results": out}))
+    return dev, torch.cuda.current_stream(dev), max(20, args.steps), peaks()
 
 
-def run_only_embedding(args):
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    import __graft_entry__
-    __graft_entry__.build()
-    print(json.dumps({"only": "vocab_embedding",
-                      "results": measure_embedding(dev, args.steps, peaks())}))
+def run_only(args):
+    import tensor_transformer_mlp_columnparallel_gb300 as tp  # noqa: F401
+    dev, stream, iters, pk = _only(args)
+    if args.only_ce:
+        res = {"only": "vocab_ce", "tokens": args.only_ce,
+               "results": measure_ce(dev, stream, iters, pk, args.only_ce)}
+    elif args.only_embedding:
+        res = {"only": "vocab_embedding", "results": measure_embedding(dev, iters, pk)}
+    else:
+        import tensor_transformer_mlp_columnparallel_gb300 as tp
+        fc = MLP_CONFIGS["mlp_bf16_gelu_n16_d12288_f49152_t8"]
+        fb = Block(fc, args.mode, dev, with_dy=False)
+        ms, _, t = _lib_timed(tp, fb.forward, iters, stream)
+        res = {"only": "decode", "mode": args.mode,
+               "results": _hbm_entry(decode_bytes(fc) / (ms * 1e-3) / 1e9, ms, pk),
+               "kernels": kernel_table(t, ms * iters)}
+    print(json.dumps(res))
 
 
 def main():
     args = parse()
-    if args.only_ce:
-        run_only_ce(args)
-        return
-    if args.only_embedding:
-        run_only_embedding(args)
+    if args.only_ce or args.only_embedding or args.only_decode:
+        run_only(args)
         return
     if args.impl == "reference":
         run_reference(args)
