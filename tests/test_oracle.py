@@ -15,7 +15,7 @@ import oracle
 from oracle import mlp as omlp
 from oracle import sharded as osh
 from oracle import ce as oce
-from workloads.gen import gen_random_mlp, gen_integer_mlp
+from workloads.gen import gen_random_mlp, gen_integer_mlp, gen_sparse_integer_mlp
 from tests.tolerance import normwise_rel_err, TOL
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -135,6 +135,28 @@ def test_shard_sum_integer_inputs_bit_exact(T, dtype):
     sh = osh.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "relu", T)
     np.testing.assert_array_equal(sh["Y"], full["Y"])
     assert np.all(np.abs(full["Y"]) < 256) and np.all(full["Y"] == np.round(full["Y"]))
+
+
+@pytest.mark.parametrize("T", [2, 4])
+def test_sparse_integer_inputs_long_k_shard_sum_bit_exact(T):
+    """The sparse {-1, 0, 1} inputs of the GPU's long-K bit-exact tests: at a
+    reduction length of 4104 every stored value stays an integer within bf16's
+    exact range, most outputs are non-zero, and the shard sum (forward) and the
+    column-shard dX sum (backward) equal the unsharded definition exactly."""
+    inp = gen_sparse_integer_mlp(N=48, D=4104, F=T * 1032, T=T, dtype="bf16", seed=7,
+                                 density=(0.25, 0.02, 0.02, 0.25), bias=True)
+    X = omlp.as_f64(inp.X)
+    assert set(np.unique(X)) <= {-1.0, 0.0, 1.0}
+    assert 0.2 < np.mean(X != 0) < 0.3 and 0.015 < np.mean(omlp.as_f64(inp.W1) != 0) < 0.025
+    full = omlp.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "relu")
+    sh = osh.forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "relu", T)
+    np.testing.assert_array_equal(sh["Y"], full["Y"])
+    g = omlp.backward(inp.X, inp.W1, inp.b1, inp.W2, inp.dY, "relu")
+    gs = osh.backward_dx(inp.X, inp.W1, inp.b1, inp.W2, inp.dY, "relu", T)
+    np.testing.assert_array_equal(gs["dX"], g["dX"])
+    for v in (full["Z"], full["Y"], g["dZ"], g["dX"], g["dW1"], g["dW2"], g["db1"]):
+        assert np.all(v == np.round(v)) and np.max(np.abs(v)) <= 256
+    assert np.mean(full["Y"] != 0) > 0.5
 
 
 @pytest.mark.parametrize("T", [2, 4, 8])

@@ -251,15 +251,17 @@ def test_d4096_f16384_t4_forward_full_size_sampled(mode):
     assert_close(cat_cols([h[rows] for h in H]), f["H"], "bf16", "H rows")
 
 
-def test_d8192_f28672_t8_forward_backward_full_size_sampled():
-    """The fwd+bwd workload, in the launch configuration the benchmark times
-    (split-K shard sum, no bias): sampled rows of Y and dX, sampled hidden
-    units of dW1 (columns) and dW2 (rows)."""
+@pytest.mark.parametrize("mode", MODES)
+def test_d8192_f28672_t8_forward_backward_full_size_sampled(mode):
+    """The fwd+bwd workload in both block-end modes (split-K shard sum: the
+    launch configuration the benchmark's headline times; T fp32 partials and
+    the reduce: its PARTIALS figure), no bias: sampled rows of Y and dX,
+    sampled hidden units of dW1 (columns) and dW2 (rows)."""
     cfg = MLP_CONFIGS["mlp_bf16_gelu_n8192_d8192_f28672_t8_fwdbwd"]
     inp = gen_mlp_inputs(cfg)
     gp = to_gpu(inp)
-    Y, H, Z = run_forward(gp, cfg.act, "splitk")
-    dX, dW1, dW2, _, _ = run_backward(gp, H, Z, cfg.act, "splitk", bias_grads=False)
+    Y, H, Z = run_forward(gp, cfg.act, mode)
+    dX, dW1, dW2, _, _ = run_backward(gp, H, Z, cfg.act, mode, bias_grads=False)
     torch.cuda.synchronize()
     rows = _rows(inp.N, 48, 2)
     f = oracle.mlp.forward_rows(inp.X, inp.W1, None, inp.W2, None, cfg.act, rows)

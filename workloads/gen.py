@@ -179,6 +179,34 @@ def gen_integer_mlp(N: int, D: int, F: int, T: int, dtype: str, bias: bool, seed
     return MLPInputs(X=X, W1=W1, W2=W2, b1=b1, b2=b2, dY=dY, T=T, act="relu", dtype=dtype)
 
 
+def gen_sparse_integer_mlp(N: int, D: int, F: int, T: int, dtype: str, seed: int,
+                           density=(0.1, 0.02, 0.02, 0.04), bias: bool = False,
+                           with_dy: bool = True) -> MLPInputs:
+    """Sparse entries in {-1, 0, 1}: each entry of X, W1, W2 and dY (in that
+    order of `density`) is non-zero with the given probability, with sign +1
+    or -1 equally likely; biases, if any, from {-2..2}. At long reduction
+    lengths (thousands) the sparsity keeps every sum a small integer, so
+    sharded and unsharded results stay comparable bit for bit while most
+    outputs are non-zero. The caller checks the magnitudes it relies on."""
+    pX, pW1, pW2, pdY = density
+
+    def sparse(shape, name, p):
+        g = _gen(seed, name)
+        keep = torch.rand(shape, generator=g) < p
+        sign = torch.randint(0, 2, shape, generator=g) * 2 - 1
+        return (keep.to(torch.int64) * sign).to(_storage(dtype))
+
+    def ints(shape, name, lo, hi):
+        return torch.randint(lo, hi + 1, shape, generator=_gen(seed, name)).to(_storage(dtype))
+    X = sparse((N, D), "X", pX)
+    W1 = sparse((D, F), "W1", pW1)
+    W2 = sparse((F, D), "W2", pW2)
+    b1 = ints((F,), "b1", -2, 2) if bias else None
+    b2 = ints((D,), "b2", -2, 2) if bias else None
+    dY = sparse((N, D), "dY", pdY) if with_dy else None
+    return MLPInputs(X=X, W1=W1, W2=W2, b1=b1, b2=b2, dY=dY, T=T, act="relu", dtype=dtype)
+
+
 @dataclass
 class CEInputs:
     logits: torch.Tensor    # [N, V] float32
