@@ -238,6 +238,13 @@ tpmlp_status tpmlp_vocab_ce_backward(int64_t N, int64_t V, int T, const float* l
  * - Shapes must satisfy T * round_up(N*D*4, 256) <= TPMLP_NOALLOC_SCRATCH_BYTES
  *   (e.g. T = 8, N = 16, D = 12288); larger ones return TPMLP_ERR_WORKSPACE
  *   and launch nothing.
+ * - The array serves as a workspace of TPMLP_NOALLOC_SCRATCH_BYTES, so the
+ *   launch plans are those tpmlp_forward picks with a workspace of that size:
+ *   the few-token GEMMs take the stream-K form only where its scratch fits
+ *   behind the partials (small blocks such as N = 8, D = 2048, F/T = 128);
+ *   wider few-token shapes such as T = 8, N = 16, D = 12288 run whole tiles
+ *   or the cluster K split, which their plans prefer with or without the
+ *   scratch.
  * - The first call on each device looks up the array's device address with
  *   that device current; make that first call before any stream capture.
  * - All calls share the one array. Calls whose GPU work can overlap (other
@@ -293,6 +300,21 @@ void tpmlp_set_wait_timeout_ns(uint64_t ns);
  * always runs out after `timeout_ns`. The caller then sees TPMLP_ERR_TIMEOUT
  * from tpmlp_check_device_error(). */
 tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Failure-detection self test of the tensor-core GEMM (page "一层 MLP 太宽而放
+ * 不下时怎样切？", §11: a collective that waits forever, found by numbering
+ * and timing the waits). While `role` is 1, 2 or 3, every bf16 GEMM launch
+ * makes that role of each of its CTAs (1: the epilogue warps, 2: the
+ * MMA-issuing thread, 3: the TMA-issuing thread) first wait, with the bounded
+ * wait of tpmlp_set_wait_timeout_ns, on a barrier that nothing completes.
+ * The wait runs out; the kernel records TPMLP_ERR_TIMEOUT in the device
+ * error word, raises its abort flag, and every role leaves through the same
+ * exit as after a real timeout: the copies and MMAs already issued are
+ * waited for, tensor memory is freed, the CTAs of a cluster leave together.
+ * The outputs of such a launch are undefined. 0 (the default) turns the stall
+ * off; other values return TPMLP_ERR_ARG. Process-wide; set it only while no
+ * other thread launches GEMMs. Library extension for tests. */
+tpmlp_status tpmlp_selftest_gemm_stall(int role);
 
 /* ---- instrumentation ---------------------------------------------------- */
 
