@@ -465,11 +465,14 @@ def decode_bytes(fc):
 
 
 def _lib_timed(tp, fn, iters, stream, warmup=3):
-    """Per-call median ms of fn, the timed region in s and the library's
-    per-kernel records over the timed calls."""
+    """Per-call median ms of fn and the timed region in s, from event pairs
+    around each call only (no events between the call's launches), then the
+    library's per-kernel records (CUDA events around every launch, on its
+    stream) over a second pass of `iters` calls."""
+    region, per = timed_steps(fn, iters, warmup, 1, stream)
     tp.tpmlp_timing_reset()
     tp.tpmlp_timing_enable(True)
-    region, per = timed_steps(fn, iters, warmup, 1, stream, reset=tp.tpmlp_timing_reset)
+    timed_steps(fn, iters, 0, 1, stream)
     tp.tpmlp_timing_enable(False)
     return float(np.median(per)), region * 1e-3, tp.tpmlp_timing_read()
 

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     tpmlp_forward_reduce_scatter,
     tpmlp_gemm_plan,
     tpmlp_launch_count,
+    tpmlp_selftest_gemm_stall,
     tpmlp_selftest_wait_timeout,
     tpmlp_set_wait_timeout_ns,
     tpmlp_swiglu_forward,

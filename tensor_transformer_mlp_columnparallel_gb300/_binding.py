@@ -66,6 +66,7 @@ _SIGNATURES = {
     "tpmlp_check_device_error": (_int, [_vp]),
     "tpmlp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "tpmlp_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
+    "tpmlp_selftest_gemm_stall": (_int, [_int]),
     "tpmlp_launch_count": (ctypes.c_int64, []),
     "tpmlp_gemm_plan": (_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _int, _int, _int,
                                _int, ctypes.POINTER(_int), ctypes.POINTER(_int),
@@ -301,6 +302,13 @@ def tpmlp_set_wait_timeout_ns(ns: int):
 def tpmlp_selftest_wait_timeout(timeout_ns: int, device=None):
     s = torch.cuda.current_stream(device).cuda_stream
     _check(lib().tpmlp_selftest_wait_timeout(int(timeout_ns), ctypes.c_void_p(s)))
+
+
+def tpmlp_selftest_gemm_stall(role: int):
+    """While role is 1 (epilogue), 2 (MMA issuer) or 3 (TMA producer), every
+    bf16 GEMM launch makes that role stall on a barrier nothing completes
+    until the bounded wait runs out; 0 turns it off."""
+    _check(lib().tpmlp_selftest_gemm_stall(int(role)))
 
 
 def tpmlp_launch_count() -> int:

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -37,6 +38,7 @@ std::mutex g_dev_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_gemm_stall{0};
 std::atomic<int64_t> g_launches{0};
 
 int current_device() {
@@ -59,6 +61,18 @@ int* device_error_word() {
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int gemm_stall_role() { return g_gemm_stall.load(); }
+
+bool pdl_enabled() {
+    // TPMLP_PDL=0 in the environment launches every kernel fully serialized
+    // after the previous one (for A/B timing, or tools that need it)
+    static const bool on = [] {
+        const char* v = getenv("TPMLP_PDL");
+        return v == nullptr || strcmp(v, "0") != 0;
+    }();
+    return on;
+}
 
 int device_sm_count() {
     const int d = current_device();
@@ -285,6 +299,7 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
         const size_t stride = round256((size_t)N * D * 4);
         const float* parts[kMaxG];
         GemmProblem row = problem((int)N, (int)D, Fs, T, 0, Fs, 0, D, 1, "row_gemm_partials");
+        row.pre_b = N <= 64;   // W2 streams while the column GEMM finishes
         row.epi.kind = EPI_STORE;
         row.epi.out_f32 = 1;
         row.epi.ldc = D;
@@ -302,6 +317,7 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
     } else {
         GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1,
                                   Y_rows ? "row_gemm_splitk_bias_scatter" : "row_gemm_splitk_bias");
+        row.pre_b = N <= 64;   // W2 streams while the column GEMM finishes
         row.epi.kind = EPI_STORE;
         row.epi.out_f32 = f32;
         row.epi.ldc = D;
@@ -691,6 +707,12 @@ void tpmlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1
 
 tpmlp_status tpmlp_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
     return run_selftest_wait(timeout_ns, static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_selftest_gemm_stall(int role) {
+    if (role < 0 || role > 3) return TPMLP_ERR_ARG;
+    g_gemm_stall.store(role);
+    return TPMLP_OK;
 }
 
 int64_t tpmlp_launch_count(void) { return g_launches.load(); }

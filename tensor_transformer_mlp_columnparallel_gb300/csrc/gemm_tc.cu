@@ -84,9 +84,10 @@ struct Cfg {
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 3;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 5;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-    static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+    // barriers, then the TMEM address, the abort flag and the pair's load count
+    static_assert(NUM_BARS * 8 + 12 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
     static_assert(B_ROWS % BOX_MN == 0, "MN-major B boxes");
@@ -120,6 +121,11 @@ struct TcParams {
     EpiArgs epi;
     int* err;
     uint64_t timeout_ns;
+    uint64_t drain_ns;   // limit of the waits for copies and MMAs already in flight
+    int inject;          // failure-detection self test: the role that stalls (0: none)
+    int pre_b;           // 1: issue B's first stages and L2 prefetches before waiting on
+                         // the previous kernel (B is not written by it)
+    int pf_kblocks;      // k-blocks of B prefetched into L2 before that wait
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -417,10 +423,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // the odd CTA of a pair writes the number of loads it issued here (even CTA)
+    volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
     const uint32_t bar0 = smem_u32(bars);
-    // barrier indices
+    // barrier indices; STALL is never completed (the self test's stall waits on
+    // it), XCNT carries the odd CTA's load count to the even CTA
     const int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = TFULL + ACC_BUFS,
-              DRAIN = TEMPTY + ACC_BUFS, RFREE = DRAIN + 1, RFULL = DRAIN + 2;
+              DRAIN = TEMPTY + ACC_BUFS, RFREE = DRAIN + 1, RFULL = DRAIN + 2, STALL = DRAIN + 3,
+              XCNT = DRAIN + 4;
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -449,6 +459,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         mbar_init(bar(DRAIN), 1);
         mbar_init(bar(RFREE), 1);                                  // leader: stages free
         mbar_init(bar(RFULL), ks > 1 ? (ks - 1) * red_warps * 32 : 1);   // every peer lane
+        mbar_init(bar(STALL), 1);
+        mbar_init(bar(XCNT), 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -474,6 +486,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (clustered) cluster_sync();   // peer barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The next kernel on the stream may start its own set-up now (it waits
+    // for this one before touching what this one writes). Every thread but
+    // the TMA producer waits here for the kernels this one depends on; the
+    // producer waits after the weight prefetch of a weight-streaming row GEMM.
+    pdl_launch_dependents();
+    if (warp != 0 || lane != 0) pdl_wait();
 
     const int kb_per_group = p.k_blocks;
     const int kb_total = p.fold ? p.G * kb_per_group : kb_per_group;
@@ -491,10 +509,106 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             // even CTA's full barrier
             const uint32_t full0 = PAIR ? mapa_shared(bar(FULL), 0) : bar(FULL);
             const int k_group = kb_per_group * C::BK;   // K extent of one shard
+            // Loads of one k-block into stage st: the A box(es) and / or the B
+            // box(es) of shard gk at K offset k0, completing on the stage's
+            // full barrier.
+            auto issue = [&](int st, int gk, int k0, int am0, int bn0, int n0, bool do_a, bool do_b) {
+                const uint32_t fb = full0 + 8u * (uint32_t)st;
+                const uint32_t a_dst = sA0 + st * C::A_BYTES;
+                const uint32_t b_dst = sB0 + st * C::B_BYTES;
+                auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+                    if constexpr (PAIR)
+                        tma_load_2d_pair(dst, m, fb, x, y);
+                    else
+                        tma_load_2d(dst, m, fb, x, y);
+                };
+                auto load3 = [&](uint32_t dst, const CUtensorMap* m, int x, int y, int z) {
+                    if constexpr (PAIR)
+                        tma_load_3d_pair(dst, m, fb, x, y, z);
+                    else
+                        tma_load_3d(dst, m, fb, x, y, z);
+                };
+                if (do_a) {
+                    if (!p.a_mn) {
+#pragma unroll
+                        for (int h = 0; h < C::BK / BKB; ++h)
+                            load(a_dst + h * C::A_SUB, &p.tmA[gk], k0 + h * BKB, am0);
+                    } else if (p.a_3d) {
+                        load3(a_dst, &p.tmA[gk], 0, k0, am0 / BOX_MN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / BOX_MN; ++j)
+                            load(a_dst + j * C::MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
+                    }
+                }
+                if (!do_b) return;
+                // `rows` B rows (N index) starting at n_start from map m into dst
+                auto load_b = [&](uint32_t dst, const CUtensorMap* m, int n_start, int rows) {
+                    if (!p.b_mn) {
+#pragma unroll
+                        for (int h = 0; h < C::BK / BKB; ++h)
+                            load(dst + h * C::B_SUB, m, k0 + h * BKB, n_start);
+                    } else if (p.b_3d) {
+                        load3(dst, m, 0, k0, n_start / BOX_MN);
+                    } else {
+                        for (int j = 0; j < rows / BOX_MN; ++j)
+                            load(dst + j * C::MN_BOX_BYTES, m, n_start + j * BOX_MN, k0);
+                    }
+                };
+                if (!p.dual) {
+                    load_b(b_dst, &p.tmB[gk], bn0, C::B_ROWS);
+                } else if constexpr (PAIR) {
+                    // the even CTA stages the gate rows, the odd CTA the up rows
+                    load_b(b_dst, rank == 0 ? &p.tmB[gk] : &p.tmB2[gk], n0 / 2, BN / 2);
+                } else {
+                    load_b(b_dst, &p.tmB[gk], n0 / 2, BN / 2);
+                    load_b(b_dst + (BN / 2) * (p.b_mn ? C::BK : BKB) * 2, &p.tmB2[gk], n0 / 2, BN / 2);
+                }
+            };
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
-            bool ok = true;
+            bool ok = p.inject != 3 || wait_bounded(bar(STALL), 0, abort_flag, p.err, p.timeout_ns, true);
+            // Weight-streaming row GEMM: its B operand (the weights) is written
+            // by no kernel of the call, so while the column GEMM that writes A
+            // still runs, the first stages get their B boxes and the next
+            // pf_kblocks k-blocks of B are prefetched into L2; A follows the
+            // wait. (`pre` k-blocks have their stage armed and B issued.)
+            uint32_t pre = 0;
+            if (ok && p.pre_b) {
+                Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total);
+                if (w.valid()) {
+                    int g, m0, n0;
+                    decode_tile<BN, C::TILE_M>(p, w.t, g, m0, n0);
+                    const int bn0 = n0 + (int)rank * C::B_ROWS;
+                    int gk = p.fold ? w.kb0 / kb_per_group : g;
+                    int k0 = (p.fold ? w.kb0 - (w.kb0 / kb_per_group) * kb_per_group : w.kb0) * C::BK;
+                    int pf = 0;
+                    for (int kb = w.kb0; kb < w.kb1 && (pre < (uint32_t)C::STAGES || pf < p.pf_kblocks);
+                         ++kb, k0 += C::BK) {
+                        if (k0 == k_group) {
+                            k0 = 0;
+                            ++gk;
+                        }
+                        if (pre < (uint32_t)C::STAGES) {
+                            if (leader) mbar_arrive_expect_tx(bar(FULL + (int)pre), C::CTAS * C::STAGE_BYTES);
+                            issue((int)pre, gk, k0, 0, bn0, n0, false, true);
+                            ++pre;
+                        } else if (!p.b_mn) {
+                            for (int h = 0; h < C::BK / BKB; ++h) tma_prefetch_l2_2d(&p.tmB[gk], k0 + h * BKB, bn0);
+                            ++pf;
+                        } else if (p.b_3d) {
+                            tma_prefetch_l2_3d(&p.tmB[gk], 0, k0, bn0 / BOX_MN);
+                            ++pf;
+                        } else {
+                            for (int j = 0; j < C::B_ROWS / BOX_MN; ++j)
+                                tma_prefetch_l2_2d(&p.tmB[gk], bn0 + j * BOX_MN, k0);
+                            ++pf;
+                        }
+                    }
+                }
+            }
+            pdl_wait();
             for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); ok && w.valid(); w.next()) {
                 const int t = w.t;
                 int g, m0, n0;
@@ -509,58 +623,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         k0 = 0;
                         ++gk;
                     }
-                    if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full0 + 8u * (uint32_t)s;
-                    if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
-                    const uint32_t a_dst = sA0 + s * C::A_BYTES;
-                    const uint32_t b_dst = sB0 + s * C::B_BYTES;
-                    auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
-                        if constexpr (PAIR)
-                            tma_load_2d_pair(dst, m, fb, x, y);
-                        else
-                            tma_load_2d(dst, m, fb, x, y);
-                    };
-                    auto load3 = [&](uint32_t dst, const CUtensorMap* m, int x, int y, int z) {
-                        if constexpr (PAIR)
-                            tma_load_3d_pair(dst, m, fb, x, y, z);
-                        else
-                            tma_load_3d(dst, m, fb, x, y, z);
-                    };
-                    if (!p.a_mn) {
-#pragma unroll
-                        for (int h = 0; h < C::BK / BKB; ++h)
-                            load(a_dst + h * C::A_SUB, &p.tmA[gk], k0 + h * BKB, am0);
-                    } else if (p.a_3d) {
-                        load3(a_dst, &p.tmA[gk], 0, k0, am0 / BOX_MN);
+                    if (issued < pre) {   // stage armed and B issued before the wait
+                        issue(s, gk, k0, am0, bn0, n0, true, false);
                     } else {
-#pragma unroll
-                        for (int j = 0; j < BM / BOX_MN; ++j)
-                            load(a_dst + j * C::MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
-                    }
-                    // `rows` B rows (N index) starting at n_start from map m into dst
-                    auto load_b = [&](uint32_t dst, const CUtensorMap* m, int n_start, int rows) {
-                        if (!p.b_mn) {
-#pragma unroll
-                            for (int h = 0; h < C::BK / BKB; ++h)
-                                load(dst + h * C::B_SUB, m, k0 + h * BKB, n_start);
-                        } else if (p.b_3d) {
-                            load3(dst, m, 0, k0, n_start / BOX_MN);
-                        } else {
-                            for (int j = 0; j < rows / BOX_MN; ++j)
-                                load(dst + j * C::MN_BOX_BYTES, m, n_start + j * BOX_MN, k0);
+                        if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                            ok = false;
+                            break;
                         }
-                    };
-                    if (!p.dual) {
-                        load_b(b_dst, &p.tmB[gk], bn0, C::B_ROWS);
-                    } else if constexpr (PAIR) {
-                        // the even CTA stages the gate rows, the odd CTA the up rows
-                        load_b(b_dst, rank == 0 ? &p.tmB[gk] : &p.tmB2[gk], n0 / 2, BN / 2);
-                    } else {
-                        load_b(b_dst, &p.tmB[gk], n0 / 2, BN / 2);
-                        load_b(b_dst + (BN / 2) * (p.b_mn ? C::BK : BKB) * 2, &p.tmB2[gk], n0 / 2, BN / 2);
+                        if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
+                        issue(s, gk, k0, am0, bn0, n0, true, true);
                     }
                     ++issued;
                     if (++s == C::STAGES) {
@@ -569,20 +640,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     }
                 }
             }
-            // Drain: the even CTA waits until every stage it armed has landed
-            // (its full barriers count the odd CTA's bytes too), so no TMA write
-            // is in flight when the pair leaves (the final cluster barrier holds
-            // the odd CTA until then).
+            // Drain: no TMA write may still be in flight into either CTA's
+            // shared memory when the CTA (pair) leaves. Load j of a CTA went to
+            // stage j % STAGES and completes phase j / STAGES of its full
+            // barrier; the phases before the last STAGES loads completed before
+            // those loads could be issued. In a pair both CTAs' bytes complete
+            // on the even CTA's barrier, and after an abort the two CTAs may
+            // have issued different numbers of loads, so the odd CTA reports
+            // its count and the even CTA settles every phase either of them
+            // issued into: it arms the phases only the odd CTA issued (for the
+            // odd CTA's bytes) and marks as done the bytes of the phases only
+            // it issued, then waits for each phase. The final cluster barrier
+            // holds the odd CTA until then.
+            uint32_t issued_peer = issued;
+            if constexpr (PAIR) {
+                if (!leader) {
+                    st_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0u), issued);
+                    mbar_arrive_cluster(mapa_shared(bar(XCNT), 0u));   // release: the count
+                } else if (wait_bounded(bar(XCNT), 0, abort_flag, p.err, p.timeout_ns + p.drain_ns, false) &&
+                           mbar_try_wait_cluster(bar(XCNT), 0)) {
+                    issued_peer = *peer_issued;
+                }
+            }
             if (leader) {
-                const uint32_t outstanding = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
-                for (uint32_t i = 0; i < outstanding; ++i) {
-                    if (s == 0) {
-                        s = C::STAGES - 1;
-                        ph ^= 1u;
-                    } else {
-                        --s;
-                    }
-                    wait_bounded(bar(FULL + s), ph, abort_flag, p.err, p.timeout_ns, false);
+                const uint32_t hi = issued > issued_peer ? issued : issued_peer;
+                const uint32_t lo = hi > (uint32_t)C::STAGES ? hi - (uint32_t)C::STAGES : 0u;
+                for (uint32_t j = lo; j < hi; ++j) {
+                    const int sj = (int)(j % (uint32_t)C::STAGES);
+                    if (PAIR && j >= issued) mbar_arrive_expect_tx(bar(FULL + sj), C::STAGE_BYTES);
+                    if (PAIR && j >= issued_peer) mbar_complete_tx(bar(FULL + sj), C::STAGE_BYTES);
+                    wait_bounded(bar(FULL + sj), (j / (uint32_t)C::STAGES) & 1u, abort_flag, p.err,
+                                 p.drain_ns, false);
                 }
             }
         }
@@ -605,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t ph = 0;
             int acc = 0;
             uint32_t aph = 0;
-            bool ok = true;
+            bool ok = p.inject != 2 || wait_bounded(bar(STALL), 0, abort_flag, p.err, p.timeout_ns, true);
             for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); ok && w.valid(); w.next()) {
                 if (!wait_fast(bar(TEMPTY + acc), aph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                     ok = false;
@@ -658,7 +746,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 tc_commit_pair(bar(DRAIN));
             else
                 tc_commit(bar(DRAIN));
-            wait_bounded(bar(DRAIN), 0, abort_flag, p.err, p.timeout_ns, false);
+            wait_bounded(bar(DRAIN), 0, abort_flag, p.err, p.drain_ns, false);
         }
     } else {
         // ---------------- epilogue (warps 2..5 of each CTA) ----------------
@@ -668,7 +756,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         int acc = 0;
         uint32_t aph = 0;
         uint32_t rph = 0;   // K split: phase of the exchange barriers
-        for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); w.valid(); w.next()) {
+        int live = 1;
+        if (p.inject == 1) {
+            if (lane == 0) live = wait_bounded(bar(STALL), 0, abort_flag, p.err, p.timeout_ns, true);
+            live = __shfl_sync(0xffffffffu, live, 0);
+        }
+        for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); live && w.valid(); w.next()) {
             const int t = w.t;
             int g, m0, n0;
             decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
@@ -1094,21 +1187,30 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     kp.epi = pr.epi;
     kp.err = device_error_word();
     kp.timeout_ns = wait_timeout_ns();
+    // copies and MMAs already issued complete in microseconds; their waits
+    // get at least 100 ms whatever the limit for waiting on other roles
+    kp.drain_ns = kp.timeout_ns > 100000000ull ? kp.timeout_ns : 100000000ull;
+    kp.inject = gemm_stall_role();
     if (kp.err == nullptr) return TPMLP_ERR_CUDA;
 
     const int cl = PAIR ? 2 : ks;   // CTAs per cluster
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
+    cfg.attrs = attr;
+    // programmatic dependent launch: the kernel may start while the previous
+    // kernel on the stream finishes (it waits for it before using its data)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = 1;
     if (cl > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cl;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     const int max_units = resident_units<BN, PAIR>(PAIR ? 2 : 1);
     if (max_units < 1) return TPMLP_ERR_CUDA;
@@ -1118,6 +1220,14 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
                          : ks > 1 ? kp.num_tiles
                                   : (kp.num_tiles < max_units ? kp.num_tiles : max_units);
     cfg.gridDim = dim3((unsigned)(units * cl));
+    if (pr.pre_b && !PAIR && !pr.dual) {
+        // about 64 MB of B prefetched into L2 over the whole grid, beyond the
+        // stages (what HBM can add while the previous kernel's last wave
+        // leaves SMs idle, and well inside L2)
+        kp.pre_b = 1;
+        const int64_t per_cta = (int64_t)64 * 1024 * 1024 / ((int64_t)units * cl * C::B_BYTES);
+        kp.pf_kblocks = (int)(per_cta > 256 ? 256 : per_cta);
+    }
     cudaError_t e;
     {
         LaunchScope ls(pr.name, s);

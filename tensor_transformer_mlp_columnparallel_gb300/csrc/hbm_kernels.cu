@@ -57,6 +57,10 @@ __device__ __forceinline__ float load_out(const void* p, int64_t i) {
 
 template <typename OutT, int NT>
 __global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParams p) {
+    // launched with programmatic stream serialization after the GEMM that
+    // writes the partials: wait for it before the first load
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t total8 = p.N * p.D / 8;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total8; i += stride) {
@@ -115,6 +119,8 @@ __global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParam
 
 template <typename OutT>
 __global__ void __launch_bounds__(256) block_reduce_scalar_kernel(const ReduceParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t total = p.N * p.D;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -131,18 +137,25 @@ __global__ void __launch_bounds__(256) block_reduce_scalar_kernel(const ReducePa
 
 template <typename OutT>
 cudaError_t launch_reduce(const ReduceParams& kp, bool vec, int grid, cudaStream_t s) {
-    if (!vec) {
-        block_reduce_scalar_kernel<OutT><<<grid, 256, 0, s>>>(kp);
-    } else {
-        switch (kp.T) {
-            case 1: block_reduce_vec_kernel<OutT, 1><<<grid, 256, 0, s>>>(kp); break;
-            case 2: block_reduce_vec_kernel<OutT, 2><<<grid, 256, 0, s>>>(kp); break;
-            case 4: block_reduce_vec_kernel<OutT, 4><<<grid, 256, 0, s>>>(kp); break;
-            case 8: block_reduce_vec_kernel<OutT, 8><<<grid, 256, 0, s>>>(kp); break;
-            default: block_reduce_vec_kernel<OutT, 0><<<grid, 256, 0, s>>>(kp); break;
-        }
+    // programmatic dependent launch: the reduce may start its CTAs while the
+    // GEMM that writes the partials finishes; the kernel waits for it first
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!vec) return cudaLaunchKernelEx(&cfg, block_reduce_scalar_kernel<OutT>, kp);
+    switch (kp.T) {
+        case 1: return cudaLaunchKernelEx(&cfg, block_reduce_vec_kernel<OutT, 1>, kp);
+        case 2: return cudaLaunchKernelEx(&cfg, block_reduce_vec_kernel<OutT, 2>, kp);
+        case 4: return cudaLaunchKernelEx(&cfg, block_reduce_vec_kernel<OutT, 4>, kp);
+        case 8: return cudaLaunchKernelEx(&cfg, block_reduce_vec_kernel<OutT, 8>, kp);
+        default: return cudaLaunchKernelEx(&cfg, block_reduce_vec_kernel<OutT, 0>, kp);
     }
-    return cudaGetLastError();
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

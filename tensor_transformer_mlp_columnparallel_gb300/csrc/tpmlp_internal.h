@@ -63,6 +63,10 @@ struct GemmProblem {
     size_t sk_part_bytes;
     int* sk_cnt;
     int64_t sk_cnt_cap;        // counters available
+    // 1: B is written by no kernel the GEMM waits for (the weights of a row
+    // GEMM that follows its call's column GEMM), so a weight-streaming launch
+    // may load and prefetch B before that wait
+    int pre_b;
 };
 
 // Stream-K scratch: at most this many CTAs share the (tile, k-block) units,
@@ -102,6 +106,8 @@ tpmlp_status run_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
 // ---- services of the API translation unit --------------------------------
 int* device_error_word();          // per current device; NULL on failure
 uint64_t wait_timeout_ns();
+int gemm_stall_role();             // failure-detection self test of the GEMM (0: off)
+bool pdl_enabled();                // programmatic dependent launch (TPMLP_PDL != 0)
 int device_sm_count();
 
 // Counts the launch and, when timing is on, brackets it with CUDA events

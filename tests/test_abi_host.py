@@ -184,3 +184,10 @@ def test_product_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "oracle/" not in src, f
+
+
+def test_gemm_stall_self_test_role_is_checked(lib):
+    assert lib.tpmlp_selftest_gemm_stall(4) == B.ERR_ARG
+    assert lib.tpmlp_selftest_gemm_stall(-1) == B.ERR_ARG
+    for role in (1, 2, 3, 0):
+        assert lib.tpmlp_selftest_gemm_stall(role) == B.OK

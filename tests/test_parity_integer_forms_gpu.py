@@ -106,14 +106,30 @@ def assert_exact(inp, out, f, g, tag):
 # tensor-core GEMMs: CTA pair and single CTA
 # ---------------------------------------------------------------------------
 
+PAIR_CANDIDATES = [(4160, 4104, 2312), (4128, 4168, 2312), (4352, 4104, 2056),
+                   (4096, 4104, 2056)]
+
+
+def pair_shape(T=2):
+    """The first (N, D, F/T), ragged against the 256-row pair tile and the
+    64-wide box where possible, whose column GEMM (and dZ GEMM, the same
+    problem), folded row GEMM (and dX GEMM) and dW2 GEMM all run as CTA pairs
+    on this device (the plan weighs waves, so ragged shapes may prefer single
+    CTAs)."""
+    for N, D, Fs in PAIR_CANDIDATES:
+        if all(tp.tpmlp_gemm_plan(M, Nn, K, T, fold=f)[1] == 2
+               for M, Nn, K, f in ((N, Fs, D, False), (N, D, Fs, True), (Fs, D, N, False))):
+            return N, D, Fs
+    raise AssertionError("no candidate shape runs every GEMM as a CTA pair")
+
+
 def test_cta_pair_128_deep_ring_long_k_ragged():
-    """N = 4160 tokens (16 pair tiles of 256 and a 64-row tail), D = 4104,
-    F/T = 2056 (neither a multiple of the 64-wide box nor of the 256-wide
-    tile): the column, dZ and dX GEMMs reduce over 4104 or 4112, the dW GEMMs
-    over 4160 tokens, all in 128-deep stages of a 3-stage ring."""
-    N, D, Fs, T = 4160, 4104, 2056, 2
-    for M, Nn, K, G, fold in ((N, Fs, D, T, 0), (N, D, Fs, T, 1), (Fs, D, N, T, 0)):
-        assert tp.tpmlp_gemm_plan(M, Nn, K, G, fold=bool(fold))[1] == 2
+    """About 4100-4350 tokens, D about 4100, F/T = 2056-2312, ragged against the
+    256-row pair tile, the 256-wide tile and the 64-wide box: the column, dZ
+    and dX GEMMs reduce over D or F, the dW GEMMs over the tokens, all more
+    than 4096 deep, in 128-deep stages of a 3-stage ring."""
+    T = 2
+    N, D, Fs = pair_shape(T)
     inp = gen_sparse_integer_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", seed=301)
     f, g = expected(inp, bias_grads=False)
     for mode in MODES:
