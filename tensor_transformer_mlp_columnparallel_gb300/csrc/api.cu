@@ -187,21 +187,29 @@ size_t dz_bytes(tpmlp_dtype dt, int64_t N, int64_t Fs, int T) {
     return (size_t)T * round256((size_t)N * Fs * (dt == TPMLP_BF16 ? 2 : 4));
 }
 
-// Optional scratch of the few-token (N <= 64) bf16 GEMMs' stream-K form: two
-// arrival counters per tile for the most tiles any GEMM of the block has
-// (T groups of up to max(F/T, D) columns in 128-column tiles), then the
-// partial-accumulator slots of as many CTAs as the GEMMs have (tile,
-// k-block) units, at most kSkMaxCtas. Every GEMM with M = N of the block
-// has T x (N-columns / 128 tiles) x (K / 64 k-blocks) units with
-// {N-columns, K} = {F/T, D}, folded or grouped alike.
+// Optional scratch of the bf16 GEMMs' stream-K form
+// (tpmlp_workspace_bytes_balanced): per-tile arrival counters, then fp32
+// partial-accumulator slots, two per CTA.
+// - N <= 64 (few tokens; every (tile, k-block) unit is dealt out): 4
+//   counters per tile for the most tiles any GEMM of the block has (T groups
+//   of up to max(F/T, D) columns in 128-column tiles), slots of
+//   round_up(N, 32) rows for as many CTAs as the GEMMs have units, at most
+//   kSkMaxCtas. Every GEMM with M = N of the block has T x (N-columns / 128
+//   tiles) x (K / 64 k-blocks) units with {N-columns, K} = {F/T, D}, folded
+//   or grouped alike.
+// - N > 64 (only the part wave's tiles are dealt out, fewer tiles than
+//   units): 8 counters (4 per CTA of a pair) for up to kSkMaxCtas tiles, slots
+//   of 128 rows for kSkMaxCtas CTAs (64 MiB).
 size_t sk_part_bytes_for(int64_t M, int64_t units) {
+    if (M > 64) return (size_t)kSkMaxCtas * 2 * 128 * kSkMaxBn * 4;
     const int64_t rows = M < 64 ? ((M + 31) / 32) * 32 : 64;
     const int64_t ctas = units < kSkMaxCtas ? units : kSkMaxCtas;
     return (size_t)ctas * 2 * (size_t)rows * kSkMaxBn * 4;
 }
-size_t sk_cnt_bytes(int64_t D, int64_t Fs, int T) {
+size_t sk_cnt_bytes(int64_t N, int64_t D, int64_t Fs, int T) {
+    if (N > 64) return round256((size_t)kSkMaxCtas * 8 * sizeof(int));
     const int64_t cols = Fs > D ? Fs : D;
-    return round256((size_t)2 * T * ((cols + 127) / 128) * sizeof(int));
+    return round256((size_t)4 * T * ((cols + 127) / 128) * sizeof(int));
 }
 int64_t sk_units_bound(int64_t D, int64_t Fs, int T) {
     const int64_t a = ((Fs + 127) / 128) * ((D + 63) / 64);
@@ -209,8 +217,8 @@ int64_t sk_units_bound(int64_t D, int64_t Fs, int T) {
     return (int64_t)T * (a > b ? a : b);
 }
 size_t sk_bytes(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T) {
-    if (dt != TPMLP_BF16 || N < 1 || N > 64) return 0;
-    return sk_cnt_bytes(D, F / T, T) + sk_part_bytes_for(N, sk_units_bound(D, F / T, T));
+    if (dt != TPMLP_BF16 || N < 1) return 0;
+    return sk_cnt_bytes(N, D, F / T, T) + sk_part_bytes_for(N, sk_units_bound(D, F / T, T));
 }
 
 struct SkArea {
@@ -229,7 +237,7 @@ SkArea sk_area(void* ws, size_t ws_bytes, size_t base, tpmlp_dtype dt, int64_t N
     const size_t off = round256(base);
     if (need == 0 || ws == nullptr || !aligned16(ws) || ws_bytes < off + need) return a;
     char* p = static_cast<char*>(ws) + off;
-    const size_t cb = sk_cnt_bytes(D, F / T, T);
+    const size_t cb = sk_cnt_bytes(N, D, F / T, T);
     a.cnt = reinterpret_cast<int*>(p);
     a.cnt_cap = (int64_t)(cb / sizeof(int));
     a.part = reinterpret_cast<float*>(p + cb);
@@ -299,7 +307,6 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
         const size_t stride = round256((size_t)N * D * 4);
         const float* parts[kMaxG];
         GemmProblem row = problem((int)N, (int)D, Fs, T, 0, Fs, 0, D, 1, "row_gemm_partials");
-        row.pre_b = N <= 64;   // W2 streams while the column GEMM finishes
         row.epi.kind = EPI_STORE;
         row.epi.out_f32 = 1;
         row.epi.ldc = D;
@@ -317,7 +324,6 @@ static tpmlp_status block_end(tpmlp_dtype dt, int64_t N, int64_t D, int T, int F
     } else {
         GemmProblem row = problem((int)N, (int)D, Fs, T, 1, Fs, 0, D, 1,
                                   Y_rows ? "row_gemm_splitk_bias_scatter" : "row_gemm_splitk_bias");
-        row.pre_b = N <= 64;   // W2 streams while the column GEMM finishes
         row.epi.kind = EPI_STORE;
         row.epi.out_f32 = f32;
         row.epi.ldc = D;
@@ -536,7 +542,7 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
         g2.B[r] = dY;
         g2.epi.C[r] = dW2[r];
     }
-    TPMLP_TRY(run_gemm(dt, g2, s));
+    TPMLP_TRY(run_gemm(dt, g2, s, sk));
 
     // 3. dW1^(r) = X^T dZ^(r): A(m, k) = X[k, m] (MN-major), B(k, n) = dZ^(r)[k, n]
     GemmProblem g3 = problem((int)D, Fs, (int)N, T, 0, D, 1, Fs, 1, "bwd_dw1_gemm");
@@ -548,7 +554,7 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
         g3.B[r] = dZ[r];
         g3.epi.C[r] = dW1[r];
     }
-    TPMLP_TRY(run_gemm(dt, g3, s));
+    TPMLP_TRY(run_gemm(dt, g3, s, sk));
 
     // 4. dX = sum_r dZ^(r) W1^(r)^T: A = dZ^(r) (K-major), B(k, n) = W1^(r)[n, k] (K-major)
     if (mode == TPMLP_REDUCE_PARTIALS) {
@@ -665,7 +671,7 @@ tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, i
         return TPMLP_ERR_SHAPE;
     GemmProblem p = problem((int)M, (int)N, (int)K, G, fold ? 1 : 0, K, 0, K, 0, "plan");
     p.dual = dual ? 1 : 0;
-    if (balanced && M <= 64) {
+    if (balanced) {
         // a scratch as large as the block's workspace would provide (never
         // dereferenced: the plan launches nothing)
         static float part_dummy;
@@ -673,7 +679,7 @@ tpmlp_status tpmlp_gemm_plan(int64_t M, int64_t N, int64_t K, int G, int fold, i
         p.sk_part = &part_dummy;
         p.sk_part_bytes = sk_part_bytes_for(M, kSkMaxCtas);
         p.sk_cnt = &cnt_dummy;
-        p.sk_cnt_cap = (int64_t)2 * G * ((N + 127) / 128);
+        p.sk_cnt_cap = M > 64 ? (int64_t)kSkMaxCtas * 8 : (int64_t)4 * G * ((N + 127) / 128);
     }
     return plan_gemm_tc(p, bn, mma_ctas, ksplit);
 }

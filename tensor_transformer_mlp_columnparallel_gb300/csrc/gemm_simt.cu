@@ -76,10 +76,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
     const int n0 = blockIdx.x * TN, m0 = blockIdx.y * TM;
     const int kr = (int)blockIdx.z % p.ks;    // rank in the K-split cluster
     const int gz = (int)blockIdx.z / p.ks;    // group (non-folded)
-    // launched with programmatic stream serialization: let the next kernel
-    // start its set-up, and wait for the previous one before reading anything
-    pdl_launch_dependents();
-    pdl_wait();
+
     float acc[4][4], acc2[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -247,21 +244,17 @@ tpmlp_status run_gemm_simt(const GemmProblem& pr, cudaStream_t s) {
     }
     kp.ks = ks;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3((unsigned)gx, gy, (unsigned)(gz * ks));
     cfg.blockDim = dim3(256);
     cfg.stream = s;
-    cfg.attrs = attr;
-    // programmatic dependent launch (the kernel waits before touching memory)
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-    cfg.numAttrs = 1;
     if (ks > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 1;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = (unsigned)ks;
-        cfg.numAttrs = 2;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)ks;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     }
     cudaError_t e;
     {

@@ -113,19 +113,18 @@ struct TcParams {
     int band;         // band width in tiles
     int ksplit;       // CTAs of a cluster sharing one tile's K range (single-CTA
                       // tiles, M <= KSPLIT_ROWS, one tile per cluster); 1 = off
-    int sk;           // 1: stream-K (see Work)
-    int sk_units;     // U = tiles x k-blocks
-    int sk_rows;      // rows of a scratch slot (32 or 64)
-    float* sk_part;   // P x 2 slots of sk_rows x BN fp32 partial accumulators
-    int* sk_cnt;      // 2 counters per tile (one per 32 rows), zero at launch
+    int sk;           // 1: stream-K phase after the whole tiles (see Work)
+    int sk_dp_tiles;  // tiles [0, sk_dp_tiles) run whole before the stream-K phase
+    int sk_units;     // U = stream-K tiles x k-blocks
+    int sk_parts;     // units taking part in the stream-K phase (the first sk_parts)
+    int sk_rows;      // rows per CTA of a scratch slot (32, 64 or 128)
+    float* sk_part;   // P x 2 x CTAS slots of sk_rows x BN fp32 partial accumulators
+    int* sk_cnt;      // 4 x CTAS counters per stream-K tile (one per 32-row warp), zero at launch
     EpiArgs epi;
     int* err;
     uint64_t timeout_ns;
     uint64_t drain_ns;   // limit of the waits for copies and MMAs already in flight
     int inject;          // failure-detection self test: the role that stalls (0: none)
-    int pre_b;           // 1: issue B's first stages and L2 prefetches before waiting on
-                         // the previous kernel (B is not written by it)
-    int pf_kblocks;      // k-blocks of B prefetched into L2 before that wait
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -193,47 +192,58 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
     n0 = nt * BN;
 }
 
-// The work items of one CTA: tiles first_tile, first_tile + step, ... with
-// the k-block range [kb_lo, kb_hi) each, or, with stream-K (few-token GEMMs:
-// single-CTA tiles, M <= KSPLIT_ROWS), the CTA's contiguous range
-// [i U / P, (i+1) U / P) of the U = tiles x k-blocks, cut at tile
-// boundaries. Every role walks the same sequence.
+// The work items of one unit (a CTA, or a CTA pair / K-split cluster): tiles
+// first_tile, first_tile + step, ... (step = the number of units) with the
+// k-block range [kb_lo, kb_hi) each. With stream-K the whole tiles stop at
+// sk_dp_tiles (full waves: every unit has the same number), and unit i < P
+// (P = sk_parts) then takes its contiguous share [i U / P, (i+1) U / P) of
+// the U = remaining tiles x k-blocks, cut at tile boundaries. (The few-token
+// GEMMs have no whole tiles and P = all units; larger GEMMs cut each
+// remaining tile into P / tiles equal K chunks.) Every role walks the same
+// sequence.
 struct Work {
     int t, kb0, kb1;   // current item: tile, k-blocks [kb0, kb1)
-    int u, u_end;      // stream-K: next unit, end of the CTA's units
-    int kb_total, step, ntiles;
-    bool sk;
+    int u, u_end;      // stream-K: next unit (counted from the first stream-K tile), end
+    int kb_total, step, dp_tiles;
+    bool sk, has_sk;
     __device__ __forceinline__ Work(const TcParams& p, int first_tile, int tile_step, int kb_lo,
                                     int kb_hi, int kbt)
         : t(first_tile), kb0(kb_lo), kb1(kb_hi), u(0), u_end(0), kb_total(kbt), step(tile_step),
-          ntiles(p.num_tiles), sk(p.sk != 0) {
-        if (sk) {
-            u = (int)((int64_t)blockIdx.x * p.sk_units / gridDim.x);
-            u_end = (int)((int64_t)(blockIdx.x + 1) * p.sk_units / gridDim.x);
-            load();
+          dp_tiles(p.sk ? p.sk_dp_tiles : p.num_tiles), sk(false), has_sk(p.sk != 0) {
+        if (has_sk && first_tile < p.sk_parts) {
+            u = (int)((int64_t)first_tile * p.sk_units / p.sk_parts);
+            u_end = (int)((int64_t)(first_tile + 1) * p.sk_units / p.sk_parts);
         }
+        if (t >= dp_tiles) enter_sk();
+    }
+    __device__ __forceinline__ void enter_sk() {
+        sk = has_sk;
+        if (sk) load();
     }
     __device__ __forceinline__ void load() {
         if (u < u_end) {
-            t = u / kb_total;
-            kb0 = u - t * kb_total;
+            const int tl = u / kb_total;
+            t = dp_tiles + tl;
+            kb0 = u - tl * kb_total;
             kb1 = min(kb_total, kb0 + (u_end - u));
         }
     }
-    __device__ __forceinline__ bool valid() const { return sk ? u < u_end : t < ntiles; }
+    __device__ __forceinline__ bool valid() const { return sk ? u < u_end : t < dp_tiles; }
     __device__ __forceinline__ void next() {
         if (sk) {
             u += kb1 - kb0;
             load();
         } else {
             t += step;
+            if (t >= dp_tiles) enter_sk();
         }
     }
     // a stream-K item that covers only part of its tile's K range
     __device__ __forceinline__ bool partial() const { return sk && (kb0 > 0 || kb1 < kb_total); }
 };
 
-// stream-K: the CTA whose range holds unit x, and the tile of CTA c's first unit
+// stream-K: the unit whose range holds k-block unit x, and the stream-K tile
+// (counted from the first) of unit c's first k-block unit
 __device__ __forceinline__ int sk_cta_of(int64_t x, int64_t U, int P) {
     return (int)(((x + 1) * P - 1) / U);
 }
@@ -486,11 +496,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (clustered) cluster_sync();   // peer barriers initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // The next kernel on the stream may start its own set-up now (it waits
-    // for this one before touching what this one writes). Every thread but
-    // the TMA producer waits here for the kernels this one depends on; the
-    // producer waits after the weight prefetch of a weight-streaming row GEMM.
-    pdl_launch_dependents();
+    // Launched with programmatic stream serialization: the CTAs may start
+    // while the previous kernel on the stream winds down; nothing that kernel
+    // writes is touched before this wait. (The GEMM does not trigger its own
+    // dependents early: CTAs of the next kernel starting on SMs this grid
+    // frees, while its last wave still streams, measured slower.)
     if (warp != 0 || lane != 0) pdl_wait();
 
     const int kb_per_group = p.k_blocks;
@@ -509,10 +519,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             // even CTA's full barrier
             const uint32_t full0 = PAIR ? mapa_shared(bar(FULL), 0) : bar(FULL);
             const int k_group = kb_per_group * C::BK;   // K extent of one shard
-            // Loads of one k-block into stage st: the A box(es) and / or the B
-            // box(es) of shard gk at K offset k0, completing on the stage's
-            // full barrier.
-            auto issue = [&](int st, int gk, int k0, int am0, int bn0, int n0, bool do_a, bool do_b) {
+            // Loads of one k-block into stage st: the A and B boxes of shard gk
+            // at K offset k0, completing on the stage's full barrier.
+            auto issue = [&](int st, int gk, int k0, int am0, int bn0, int n0) {
                 const uint32_t fb = full0 + 8u * (uint32_t)st;
                 const uint32_t a_dst = sA0 + st * C::A_BYTES;
                 const uint32_t b_dst = sB0 + st * C::B_BYTES;
@@ -528,20 +537,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     else
                         tma_load_3d(dst, m, fb, x, y, z);
                 };
-                if (do_a) {
-                    if (!p.a_mn) {
+                if (!p.a_mn) {
 #pragma unroll
-                        for (int h = 0; h < C::BK / BKB; ++h)
-                            load(a_dst + h * C::A_SUB, &p.tmA[gk], k0 + h * BKB, am0);
-                    } else if (p.a_3d) {
-                        load3(a_dst, &p.tmA[gk], 0, k0, am0 / BOX_MN);
-                    } else {
+                    for (int h = 0; h < C::BK / BKB; ++h)
+                        load(a_dst + h * C::A_SUB, &p.tmA[gk], k0 + h * BKB, am0);
+                } else if (p.a_3d) {
+                    load3(a_dst, &p.tmA[gk], 0, k0, am0 / BOX_MN);
+                } else {
 #pragma unroll
-                        for (int j = 0; j < BM / BOX_MN; ++j)
-                            load(a_dst + j * C::MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
-                    }
+                    for (int j = 0; j < BM / BOX_MN; ++j)
+                        load(a_dst + j * C::MN_BOX_BYTES, &p.tmA[gk], am0 + j * BOX_MN, k0);
                 }
-                if (!do_b) return;
                 // `rows` B rows (N index) starting at n_start from map m into dst
                 auto load_b = [&](uint32_t dst, const CUtensorMap* m, int n_start, int rows) {
                     if (!p.b_mn) {
@@ -569,45 +575,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = p.inject != 3 || wait_bounded(bar(STALL), 0, abort_flag, p.err, p.timeout_ns, true);
-            // Weight-streaming row GEMM: its B operand (the weights) is written
-            // by no kernel of the call, so while the column GEMM that writes A
-            // still runs, the first stages get their B boxes and the next
-            // pf_kblocks k-blocks of B are prefetched into L2; A follows the
-            // wait. (`pre` k-blocks have their stage armed and B issued.)
-            uint32_t pre = 0;
-            if (ok && p.pre_b) {
-                Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total);
-                if (w.valid()) {
-                    int g, m0, n0;
-                    decode_tile<BN, C::TILE_M>(p, w.t, g, m0, n0);
-                    const int bn0 = n0 + (int)rank * C::B_ROWS;
-                    int gk = p.fold ? w.kb0 / kb_per_group : g;
-                    int k0 = (p.fold ? w.kb0 - (w.kb0 / kb_per_group) * kb_per_group : w.kb0) * C::BK;
-                    int pf = 0;
-                    for (int kb = w.kb0; kb < w.kb1 && (pre < (uint32_t)C::STAGES || pf < p.pf_kblocks);
-                         ++kb, k0 += C::BK) {
-                        if (k0 == k_group) {
-                            k0 = 0;
-                            ++gk;
-                        }
-                        if (pre < (uint32_t)C::STAGES) {
-                            if (leader) mbar_arrive_expect_tx(bar(FULL + (int)pre), C::CTAS * C::STAGE_BYTES);
-                            issue((int)pre, gk, k0, 0, bn0, n0, false, true);
-                            ++pre;
-                        } else if (!p.b_mn) {
-                            for (int h = 0; h < C::BK / BKB; ++h) tma_prefetch_l2_2d(&p.tmB[gk], k0 + h * BKB, bn0);
-                            ++pf;
-                        } else if (p.b_3d) {
-                            tma_prefetch_l2_3d(&p.tmB[gk], 0, k0, bn0 / BOX_MN);
-                            ++pf;
-                        } else {
-                            for (int j = 0; j < C::B_ROWS / BOX_MN; ++j)
-                                tma_prefetch_l2_2d(&p.tmB[gk], bn0 + j * BOX_MN, k0);
-                            ++pf;
-                        }
-                    }
-                }
-            }
             pdl_wait();
             for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); ok && w.valid(); w.next()) {
                 const int t = w.t;
@@ -623,16 +590,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         k0 = 0;
                         ++gk;
                     }
-                    if (issued < pre) {   // stage armed and B issued before the wait
-                        issue(s, gk, k0, am0, bn0, n0, true, false);
-                    } else {
-                        if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
-                            ok = false;
-                            break;
-                        }
-                        if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
-                        issue(s, gk, k0, am0, bn0, n0, true, true);
+                    if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
+                        ok = false;
+                        break;
                     }
+                    if (leader) mbar_arrive_expect_tx(bar(FULL + s), C::CTAS * C::STAGE_BYTES);
+                    issue(s, gk, k0, am0, bn0, n0);
                     ++issued;
                     if (++s == C::STAGES) {
                         s = 0;
@@ -845,27 +808,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 }
                 rph ^= 1u;
             } else if (w.partial()) {
-                // Stream-K: this CTA accumulated k-blocks [kb0, kb1) of the
+                // Stream-K: this unit accumulated k-blocks [kb0, kb1) of the
                 // tile. Each warp holding live rows stores its partial rows in
-                // the CTA's scratch slot for the tile (one for its first tile,
-                // one for its last) and counts itself in on the tile's
-                // counter for those rows; the warp that arrives last sums the
-                // slots of all CTAs sharing the tile in CTA order (the same
-                // order whichever warp is last, so the result does not depend
-                // on timing) and runs the epilogue. Nothing waits.
-                if (quarter < red_warps) {
-                    const int P = (int)gridDim.x;
+                // the unit's scratch slot for the tile (one for its first tile,
+                // one for its last; per CTA of a pair) and counts itself in on
+                // the tile's counter for those rows; the warp that arrives last
+                // sums the slots of all units sharing the tile in unit order
+                // (the same order whichever warp is last, so the result does
+                // not depend on timing) and runs the epilogue. Nothing waits.
+                if (quarter < p.sk_rows / 32) {
+                    const int P = p.sk_parts;
                     const int64_t U = p.sk_units;
                     const int rrow = quarter * 32 + lane;
-                    // the CTAs c_first .. c_first + n_contrib - 1 share the tile
-                    const int c_first = sk_cta_of((int64_t)t * kb_total, U, P);
-                    const int n_contrib = sk_cta_of((int64_t)(t + 1) * kb_total - 1, U, P) - c_first + 1;
+                    const int tl = t - p.sk_dp_tiles;   // stream-K tile index
+                    // the units c_first .. c_first + n_contrib - 1 share the tile
+                    const int c_first = sk_cta_of((int64_t)tl * kb_total, U, P);
+                    const int n_contrib = sk_cta_of((int64_t)(tl + 1) * kb_total - 1, U, P) - c_first + 1;
                     auto slot = [&](int k) -> float4* {
-                        const int cta = c_first + k;
-                        const int idx = 2 * cta + (sk_first_tile(cta, U, P, kb_total) == t ? 0 : 1);
-                        return reinterpret_cast<float4*>(p.sk_part + (size_t)idx * p.sk_rows * BN);
+                        const int unit = c_first + k;
+                        const int which = sk_first_tile(unit, U, P, kb_total) == tl ? 0 : 1;
+                        const size_t idx = (size_t)(2 * unit + which) * C::CTAS + rank;
+                        return reinterpret_cast<float4*>(p.sk_part + idx * p.sk_rows * BN);
                     };
-                    float4* mine = slot((int)blockIdx.x - c_first);
+                    float4* mine = slot(first_tile - c_first);
                     for (int c = 0; c < BN; c += 32) {
                         if (n0 + c >= p.N) break;
                         uint32_t r[32];
@@ -882,7 +847,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     // the count and the sum (global memory only from here)
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+                        else
+                            mbar_arrive(bar(TEMPTY + acc));
+                    }
                     released = true;
                     // release: every lane's partial rows before the count
                     __threadfence();
@@ -890,7 +860,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     int last = 0;
                     if (lane == 0) {
                         __threadfence();
-                        last = atomicAdd(p.sk_cnt + 2 * t + quarter, 1) == n_contrib - 1;
+                        int* cnt = p.sk_cnt + ((size_t)tl * C::CTAS + rank) * 4 + quarter;
+                        last = atomicAdd(cnt, 1) == n_contrib - 1;
                         if (last) __threadfence();   // acquire: the other partials
                     }
                     last = __shfl_sync(0xffffffffu, last, 0);
@@ -1080,32 +1051,71 @@ int resident_units(int cl) {
     return units[dev][cl];
 }
 
-// CTAs of a stream-K launch: every co-resident CTA, at most kSkMaxCtas and at
-// most one per (tile, k-block) unit; 0 when the device query fails.
-template <int BN>
-int sk_ctas(int64_t units) {
-    int64_t P = resident_units<BN, false>(1);
-    if (P > kSkMaxCtas) P = kSkMaxCtas;
-    if (P > units) P = units;
-    return (int)P;
-}
+// The stream-K form of a launch with BN-column tiles (PAIR: CTA-pair tiles).
+// Few-token GEMMs (M <= KSPLIT_ROWS, single CTAs): every (tile, k-block) unit
+// is dealt out, to every co-resident CTA (at most kSkMaxCtas, at most one per
+// unit). Other GEMMs: the tiles of the full waves run whole, one per unit (CTA
+// or pair) at a time, and each of the r remaining tiles (the part wave) is cut
+// into s = units / r equal K chunks run by r s units side by side. Chunk c of
+// every remaining tile runs at the same K offsets at the same time, so the
+// tiles sharing an operand panel read it together, as whole tiles do (a
+// contiguous deal of the k-blocks puts every unit at a different K offset:
+// measured slower, the part wave then streams its operands from HBM). `ok`
+// is false when the form does not apply (dual B, no scratch, no part wave,
+// fewer than two chunks) or the scratch is too small.
+struct SkShape {
+    int units = 0;          // CTAs, or CTA pairs
+    int parts = 0;          // units taking part in the stream-K phase
+    int dp_tiles = 0;       // tiles run whole before the stream-K phase
+    int64_t sk_units = 0;   // k-block units of the stream-K phase
+    int64_t sk_tiles = 0;   // tiles of the stream-K phase
+    int rows = 0;           // rows per CTA of a partial slot
+    bool ok = false;
+};
 
-// Whether stream-K applies to the problem with BN-column tiles and its
-// scratch holds what the launch needs (single-CTA tiles, M <= KSPLIT_ROWS,
-// no dual B).
-template <int BN>
-bool sk_fits(const GemmProblem& pr, int64_t tiles, int64_t units) {
-    if (pr.sk_part == nullptr || pr.sk_cnt == nullptr || pr.M > KSPLIT_ROWS || pr.dual) return false;
-    if (units > 0x7fffffff || 2 * tiles > pr.sk_cnt_cap) return false;
-    const int P = sk_ctas<BN>(units);
-    const int64_t rows = 32 * ((pr.M + 31) / 32);
-    return P >= 1 && (size_t)P * 2 * rows * BN * 4 <= pr.sk_part_bytes;
+template <int BN, bool PAIR>
+SkShape sk_shape(const GemmProblem& pr, int64_t tiles, int64_t kb_total) {
+    SkShape r;
+    if (pr.sk_part == nullptr || pr.sk_cnt == nullptr || pr.dual) return r;
+    if (pr.M <= KSPLIT_ROWS) {
+        if (PAIR) return r;
+        int64_t P = resident_units<BN, false>(1);
+        const int64_t U = tiles * kb_total;
+        if (P > kSkMaxCtas) P = kSkMaxCtas;
+        if (P > U) P = U;
+        r.units = (int)P;
+        r.parts = (int)P;
+        r.sk_units = U;
+        r.sk_tiles = tiles;
+        r.rows = 32 * ((pr.M + 31) / 32);
+    } else {
+        const int64_t P = resident_units<BN, PAIR>(PAIR ? 2 : 1);
+        if (P < 1 || tiles % P == 0) return r;
+        r.units = (int)P;
+        r.sk_tiles = tiles % P;
+        int64_t chunks = P / r.sk_tiles;
+        if (chunks > kb_total) chunks = kb_total;
+        if (chunks < 2) return SkShape();
+        r.parts = (int)(r.sk_tiles * chunks);
+        r.dp_tiles = (int)(tiles - r.sk_tiles);
+        r.sk_units = r.sk_tiles * kb_total;
+        r.rows = BM;
+    }
+    const int ctas = PAIR ? 2 : 1;
+    // every unit gets at least one k-block: the CTAs sharing a tile are then
+    // consecutive units, which the partial sums count on
+    if (r.units < 1 || r.parts < 1 || r.sk_units < r.parts || r.sk_units > 0x7fffffff ||
+        r.sk_tiles * 4 * ctas > pr.sk_cnt_cap ||
+        (size_t)r.parts * 2 * ctas * r.rows * BN * 4 > pr.sk_part_bytes)
+        return SkShape();
+    r.ok = true;
+    return r;
 }
 
 // ks > 1: split each tile's K range across a cluster of ks CTAs (single-CTA
 // tiles, M <= KSPLIT_ROWS, no dual B; one tile per cluster).
-// ks == 0: stream-K (single-CTA tiles, M <= KSPLIT_ROWS, no dual B): the
-// tiles' k-blocks are dealt out evenly to all CTAs and tiles split between
+// ks == 0: stream-K (see sk_shape; no dual B): k-blocks are dealt out evenly
+// to all units and tiles split between
 // CTAs are summed through the problem's scratch.
 template <int BN, bool PAIR>
 tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
@@ -1173,16 +1183,20 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
     if (ks > 1 && (PAIR || pr.dual || pr.M > KSPLIT_ROWS || ks > C::MAX_KSPLIT || ks > 8 ||
                    ks > (pr.fold ? G : 1) * kp.k_blocks))
         return TPMLP_ERR_SHAPE;
-    const int64_t sk_units = (int64_t)kp.num_tiles * (pr.fold ? G : 1) * kp.k_blocks;
     int sk_grid = 0;
+    size_t sk_cnt_bytes = 0;
     if (sk) {
-        if (PAIR || !sk_fits<BN>(pr, kp.num_tiles, sk_units)) return TPMLP_ERR_SHAPE;
-        sk_grid = sk_ctas<BN>(sk_units);
+        const SkShape sh = sk_shape<BN, PAIR>(pr, kp.num_tiles, (int64_t)(pr.fold ? G : 1) * kp.k_blocks);
+        if (!sh.ok) return TPMLP_ERR_SHAPE;
+        sk_grid = sh.units;
         kp.sk = 1;
-        kp.sk_units = (int)sk_units;
-        kp.sk_rows = 32 * ((pr.M + 31) / 32);
+        kp.sk_dp_tiles = sh.dp_tiles;
+        kp.sk_units = (int)sh.sk_units;
+        kp.sk_parts = sh.parts;
+        kp.sk_rows = sh.rows;
         kp.sk_part = pr.sk_part;
         kp.sk_cnt = pr.sk_cnt;
+        sk_cnt_bytes = (size_t)sh.sk_tiles * 4 * C::CTAS * sizeof(int);
     }
     kp.epi = pr.epi;
     kp.err = device_error_word();
@@ -1220,20 +1234,11 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
                          : ks > 1 ? kp.num_tiles
                                   : (kp.num_tiles < max_units ? kp.num_tiles : max_units);
     cfg.gridDim = dim3((unsigned)(units * cl));
-    if (pr.pre_b && !PAIR && !pr.dual) {
-        // about 64 MB of B prefetched into L2 over the whole grid, beyond the
-        // stages (what HBM can add while the previous kernel's last wave
-        // leaves SMs idle, and well inside L2)
-        kp.pre_b = 1;
-        const int64_t per_cta = (int64_t)64 * 1024 * 1024 / ((int64_t)units * cl * C::B_BYTES);
-        kp.pf_kblocks = (int)(per_cta > 256 ? 256 : per_cta);
-    }
     cudaError_t e;
     {
         LaunchScope ls(pr.name, s);
         // the arrival counters start at zero (a memset node inside a graph)
-        e = sk ? cudaMemsetAsync(pr.sk_cnt, 0, (size_t)kp.num_tiles * 2 * sizeof(int), s)
-               : cudaSuccess;
+        e = sk ? cudaMemsetAsync(pr.sk_cnt, 0, sk_cnt_bytes, s) : cudaSuccess;
         if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, kp);
     }
     if (e != cudaSuccess) return TPMLP_ERR_CUDA;
@@ -1265,16 +1270,19 @@ Plan choose_plan(const GemmProblem& pr) {
     // on grouped GEMMs, which have T times the tiles, it measured slower);
     // with the scratch, stream-K, whose CTAs read unrelated K ranges and
     // reach kSkEff of the HBM rate of whole tiles started together on the
-    // same weight rows.
+    // same weight rows. For M > 64 stream-K cuts only the part wave's tiles
+    // into K chunks (the full waves run whole tiles): its cost is the full
+    // waves plus one chunk and a pipeline fill of kSkFillKb k-blocks, at
+    // kSkSlow of the whole-tile rate (partial-row stores and sums).
     struct Cand {
         int bn;
         bool pair;
         int ks;
         double rate;
     };
-    // ks = 0: stream-K (M <= 64, with the scratch)
+    // ks = 0: stream-K (with the scratch)
     const Cand cands[] = {{256, true, 1, 1.08}, {256, false, 1, 1.0}, {128, false, 1, 0.85},
-                          {256, false, 0, 1.0},  {128, false, 0, 0.85},
+                          {256, true, 0, 1.08},  {256, false, 0, 1.0},  {128, false, 0, 0.85},
                           {256, false, 2, 1.0},  {256, false, 3, 1.0}, {256, false, 4, 1.0},
                           {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85}};
     const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
@@ -1284,6 +1292,8 @@ Plan choose_plan(const GemmProblem& pr) {
     constexpr double kSkEff = 0.87;
     constexpr double kStart = 5e-6;     // s: launch, set-up and pipeline fill
     constexpr double kSkFix = 2e-6;     // s: counter reset and partial-tile sums
+    constexpr double kSkFillKb = 4.0;   // M > 64: pipeline fill of a stream-K item, k-blocks
+    constexpr double kSkSlow = 1.05;
     double best = 1e300;
     int pick = 1;
     for (int i = 0; i < ncand; ++i) {
@@ -1304,14 +1314,23 @@ Plan choose_plan(const GemmProblem& pr) {
         };
         double cost;
         if (c.ks == 0) {
-            if (pr.M > KSPLIT_ROWS) continue;
-            const int64_t sku = tiles * kb_total;
-            const bool fits = c.bn == 128 ? sk_fits<128>(pr, tiles, sku) : sk_fits<256>(pr, tiles, sku);
-            if (!fits) continue;
-            const int64_t P = c.bn == 128 ? sk_ctas<128>(sku) : sk_ctas<256>(sku);
-            const double b = (double)((sku + P - 1) / P) * c.bn * BKB * 2.0;
-            const double hbm = (double)P * b / (kHbm * kSkEff), one = b / r_cta;
-            cost = kStart + kSkFix + (hbm > one ? hbm : one);
+            // the candidate's own k-block depth (128 for a pair, else 64)
+            const int64_t kbt = c.pair ? (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + 2 * BKB - 1) / (2 * BKB))
+                                       : kb_total;
+            const SkShape sh = c.pair ? sk_shape<256, true>(pr, tiles, kbt)
+                                      : c.bn == 128 ? sk_shape<128, false>(pr, tiles, kbt)
+                                                    : sk_shape<256, false>(pr, tiles, kbt);
+            if (!sh.ok) continue;
+            if (pr.M > KSPLIT_ROWS) {
+                // full waves, then one K chunk of a part-wave tile per unit
+                const double part = ((double)sh.sk_units / sh.parts + kSkFillKb) / (double)kbt * kSkSlow;
+                cost = ((double)(tiles / sh.units) + part) * 128.0 * c.bn / c.rate;
+            } else {
+                const int64_t P = sh.units;
+                const double b = (double)((sh.sk_units + P - 1) / P) * c.bn * BKB * 2.0;
+                const double hbm = (double)P * b / (kHbm * kSkEff), one = b / r_cta;
+                cost = kStart + kSkFix + (hbm > one ? hbm : one);
+            }
         } else {
             int64_t units = 0;
             if (c.bn == 128) units = resident_units<128, false>(c.ks);
@@ -1356,7 +1375,7 @@ tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
     const Plan c = choose_plan(pr);
     if (!c.ok) return TPMLP_ERR_CUDA;
     if (c.bn == 128) return launch<128, false>(pr, s, c.ks);
-    if (c.pair) return launch<256, true>(pr, s);
+    if (c.pair) return launch<256, true>(pr, s, c.ks);
     return launch<256, false>(pr, s, c.ks);
 }
 

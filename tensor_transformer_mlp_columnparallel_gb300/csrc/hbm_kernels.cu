@@ -58,7 +58,8 @@ __device__ __forceinline__ float load_out(const void* p, int64_t i) {
 template <typename OutT, int NT>
 __global__ void __launch_bounds__(256) block_reduce_vec_kernel(const ReduceParams p) {
     // launched with programmatic stream serialization after the GEMM that
-    // writes the partials: wait for it before the first load
+    // writes the partials: wait for it before the first load; the next
+    // kernel (a GEMM) may do its set-up while this one streams
     pdl_launch_dependents();
     pdl_wait();
     const int64_t total8 = p.N * p.D / 8;

@@ -236,22 +236,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// Bulk tensor prefetch of one box into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int32_t x, int32_t y,
-                                                   int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // 2-D tiled load of one box into shared memory; completion is signalled as
 // transaction bytes on mbarrier `bar`. x is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,

@@ -63,10 +63,6 @@ struct GemmProblem {
     size_t sk_part_bytes;
     int* sk_cnt;
     int64_t sk_cnt_cap;        // counters available
-    // 1: B is written by no kernel the GEMM waits for (the weights of a row
-    // GEMM that follows its call's column GEMM), so a weight-streaming launch
-    // may load and prefetch B before that wait
-    int pre_b;
 };
 
 // Stream-K scratch: at most this many CTAs share the (tile, k-block) units,

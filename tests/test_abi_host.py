@@ -82,12 +82,14 @@ def test_workspace_bytes(lib):
 
 
 def test_workspace_bytes_balanced(lib):
-    """The balanced size adds the few-token stream-K scratch (bf16, 1 <= N <= 64)
-    after the required part rounded to 256 bytes: 2 counters per 128-column
-    tile of the widest GEMM (T groups of max(F/T, D) columns), then
-    min(256, units) CTAs x 2 slots x round_up(N, 32) rows x 256 fp32
-    columns, units = T x max(ceil(F/T / 128) ceil(D / 64), ceil(D / 128)
-    ceil(F/T / 64)), the (tile, k-block) units of the block's GEMMs."""
+    """The balanced size adds the GEMMs' stream-K scratch (bf16, N >= 1) after
+    the required part rounded to 256 bytes. For 1 <= N <= 64: 4 counters per
+    128-column tile of the widest GEMM (T groups of max(F/T, D) columns), then
+    min(256, units) CTAs x 2 slots x round_up(N, 32) rows x 256 fp32 columns,
+    units = T x max(ceil(F/T / 128) ceil(D / 64), ceil(D / 128) ceil(F/T / 64)),
+    the (tile, k-block) units of the block's GEMMs. For N > 64 (the part wave
+    only): 256 x 8 counters, then 256 CTAs x 2 slots x 128 rows x 256 fp32
+    columns (64 MiB)."""
     import torch
     r256 = lambda x: (x + 255) // 256 * 256
     cdiv = lambda a, b: -(-a // b)
@@ -95,16 +97,19 @@ def test_workspace_bytes_balanced(lib):
     for D, F, T in ((1024, 8192, 4), (256, 1024, 2), (2048, 24, 3)):
         Fs = F // T
         units = T * max(cdiv(Fs, 128) * cdiv(D, 64), cdiv(D, 128) * cdiv(Fs, 64))
-        for N in (1, 16, 33, 64):
-            rows = (N + 31) // 32 * 32
-            sk = r256(2 * T * cdiv(max(Fs, D), 128) * 4) + min(256, units) * 2 * rows * 256 * 4
+        for N in (1, 16, 33, 64, 65, 4096):
+            if N <= 64:
+                rows = (N + 31) // 32 * 32
+                sk = r256(4 * T * cdiv(max(Fs, D), 128) * 4) + min(256, units) * 2 * rows * 256 * 4
+            else:
+                sk = r256(256 * 8 * 4) + 256 * 2 * 128 * 256 * 4
             for op in (0, 1):
                 for mode in ("splitk", "partials"):
                     base = B.tpmlp_workspace_bytes(op, torch.bfloat16, N, D, F, T, mode)
                     assert bal(op, torch.bfloat16, N, D, F, T, mode) == r256(base) + sk
     D, F, T = 1024, 8192, 4
-    # no scratch for fp32, for N > 64 and for N = 0
-    for args in ((torch.float32, 16), (torch.bfloat16, 65), (torch.bfloat16, 0)):
+    # no scratch for fp32 and for N = 0
+    for args in ((torch.float32, 16), (torch.float32, 4096), (torch.bfloat16, 0)):
         for mode in ("splitk", "partials"):
             assert bal(0, args[0], args[1], D, F, T, mode) == \
                 B.tpmlp_workspace_bytes(0, args[0], args[1], D, F, T, mode)

@@ -11,7 +11,8 @@ of a cluster leaving together.
 tpmlp_selftest_gemm_stall makes one role of every CTA (epilogue, MMA issuer
 or TMA producer) wait on a barrier that nothing completes, with a short
 limit, so that wait runs out on purpose. For each launch form (single CTA,
-CTA pair, cluster K split, stream-K) and each role the test checks that the
+CTA pair, cluster K split, stream-K of a few tokens, CTA pairs with the part
+wave dealt out) and each role the test checks that the
 forward returns promptly, that the device error word reads
 TPMLP_ERR_TIMEOUT (and is clear after reading), and that the next normal call
 on the same context gives exactly the result it gave before.
@@ -67,6 +68,10 @@ def forms():
     out.append(("ksplit", 17, D, 1000, 2, False))
     assert tp.tpmlp_gemm_plan(16, 1000, 1024, 2, balanced=True)[2] == 0
     out.append(("streamk", 16, 1024, 1000, 2, True))
+    # CTA pairs with the part wave cut into K chunks (16 x 8 x 2 pair tiles
+    # of the column GEMM: 3 full waves of 76 and 28 tiles in 2 chunks each)
+    assert tp.tpmlp_gemm_plan(4096, 2048, 4096, 2, balanced=True)[1:] == (2, 0)
+    out.append(("pair-streamk", 4096, 4096, 2048, 2, True))
     return out
 
 
@@ -82,7 +87,7 @@ def forward(g, mode, balanced):
 
 
 @pytest.mark.parametrize("role", sorted(ROLES))
-@pytest.mark.parametrize("form", ["pair", "single", "ksplit", "streamk"])
+@pytest.mark.parametrize("form", ["pair", "single", "ksplit", "streamk", "pair-streamk"])
 def test_stalled_role_times_out_and_the_context_survives(form, role):
     name, N, D, Fs, T, balanced = next(f for f in forms() if f[0] == form)
     inp = gen_random_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", act="gelu_tanh", bias=True,

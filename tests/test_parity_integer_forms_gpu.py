@@ -17,7 +17,9 @@ Forms, asked of the library's own plan where the choice depends on the device:
   dimension, reduction lengths 4104-4160;
 - single-CTA 128-row tiles (65-128 token rows, 64-deep stages);
 - the cluster K split of 2, 3 and 4 CTAs (at most 64 token rows, no scratch);
-- stream-K (at most 64 token rows, with the scratch);
+- stream-K (at most 64 token rows, with the scratch), and the part-wave
+  stream-K of larger GEMMs (CTA pairs or single CTAs: whole tiles for the
+  full waves, the last wave's k-blocks dealt out);
 - the fp32 GEMM's cluster K split (up to 8 CTAs per tile).
 """
 
@@ -147,6 +149,39 @@ def test_single_cta_tiles_long_k_with_biases():
     f, g = expected(inp, bias_grads=True)
     for mode in MODES:
         assert_exact(inp, run_block(inp, mode, True, True), f, g, f"single {mode}")
+
+
+def part_wave_shapes(T=2):
+    """Blocks whose folded row GEMM (more than 64 token rows) the plan runs
+    with a part wave dealt out (stream-K after the full waves), one with CTA
+    pairs and one with single-CTA tiles if the device's plans have them."""
+    found = {}
+    for N, D, Fs in ((4096, 4096, 2048), (2048, 4096, 1024), (4160, 4104, 2056), (1024, 2048, 2048),
+                     (100, 4096, 1024), (120, 2048, 2048), (96, 8192, 1024)):
+        bn, ctas, ks = tp.tpmlp_gemm_plan(N, D, Fs, T, fold=True, balanced=True)
+        if ks == 0:
+            found.setdefault(ctas, (N, D, Fs))
+    return found
+
+
+def test_part_wave_stream_k_bit_exact():
+    """The whole tiles of the full waves, then the part wave's k-blocks dealt
+    out to every unit, partial accumulators summed through the scratch in
+    unit order: equal to the oracle bit for bit, with and without the scratch
+    (the form without it runs the part wave as whole tiles)."""
+    T = 2
+    found = part_wave_shapes(T)
+    assert 2 in found, found
+    for ctas, (N, D, Fs) in sorted(found.items()):
+        dens = (0.1, 0.02, 0.02, 0.04) if N > 1000 else (0.25, 0.02, 0.02, 0.25)
+        inp = gen_sparse_integer_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", seed=340 + ctas,
+                                     density=dens, bias=True)
+        bias_grads = N <= 1000
+        f, g = expected(inp, bias_grads=bias_grads)
+        for mode in MODES:
+            for balanced in (True, False):
+                out = run_block(inp, mode, balanced, bias_grads)
+                assert_exact(inp, out, f, g, f"part wave ctas={ctas} N={N} {mode} bal={balanced}")
 
 
 # ---------------------------------------------------------------------------

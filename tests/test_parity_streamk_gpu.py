@@ -54,10 +54,18 @@ def test_plans_take_stream_k_only_with_the_scratch_and_few_rows():
     # a few tiles of a small block take it (the shapes below)
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=True)[2] == 0
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=False)[2] != 0
-    # more than 64 rows, the gated dual GEMM, and CTA pairs never take it
-    assert tp.tpmlp_gemm_plan(65, 6144, 12288, 8, balanced=True)[2] != 0
+    # the gated dual GEMM never takes it
     assert tp.tpmlp_gemm_plan(16, 6144, 12288, 8, dual=True, balanced=True)[2] != 0
-    assert tp.tpmlp_gemm_plan(4096, 4096, 4096, 4, balanced=True) == (256, 2, 1)
+    assert tp.tpmlp_gemm_plan(4096, 4096, 4096, 4, dual=True, balanced=True)[2] != 0
+    # more than 64 rows: only the part wave's tiles are cut into K chunks, so
+    # a GEMM whose pair tiles fill whole waves runs whole tiles (19 x 4 on 76
+    # pairs), one with a small part wave takes it (16 x 16 x 4 = 1024 pair
+    # tiles: 13 waves and 36 tiles in 2 chunks), and without the scratch none
+    units = 76 if tp.tpmlp_gemm_plan(19 * 256, 1024, 4096, 1, balanced=False)[1] == 2 else 0
+    if units:
+        assert tp.tpmlp_gemm_plan(19 * 256, 1024, 4096, 1, balanced=True)[2] == 1
+    assert tp.tpmlp_gemm_plan(4096, 4096, 4096, 4, balanced=True) == (256, 2, 0)
+    assert tp.tpmlp_gemm_plan(4096, 4096, 4096, 4, balanced=False) == (256, 2, 1)
 
 
 def shapes():

@@ -1,10 +1,10 @@
 """Back-to-back launches with programmatic dependent launch.
 
-Every GEMM and block-end reduce is launched so that it may start while the
-previous kernel on the stream finishes: it triggers its own dependents after
-set-up and waits (griddepcontrol.wait) before reading anything an earlier
-kernel wrote or writing anything. The weight-streaming row GEMM also loads
-and prefetches its weights before that wait. These tests queue many calls
+Every tensor-core GEMM and block-end reduce is launched so that it may start
+while the previous kernel on the stream winds down, and waits
+(griddepcontrol.wait) before reading anything an earlier kernel wrote or
+writing anything; the reduce lets the next kernel start its set-up while it
+streams. These tests queue many calls
 without synchronising, each writing fresh outputs, and require every result
 to equal the first bit for bit (a read before the producer finished, or a
 write while the consumer still reads, would show as a difference) and to
@@ -34,8 +34,8 @@ def _built():
 
 @pytest.mark.parametrize("mode", ["splitk", "partials"])
 def test_weight_streaming_forwards_back_to_back(mode):
-    """16 tokens, D = 4096, F = 8 x 2048: the row GEMM stages and prefetches
-    W2 before the column GEMM has finished; 24 forwards queued at once."""
+    """16 tokens, D = 4096, F = 8 x 2048 (the weight-streaming GEMM forms):
+    24 forwards queued at once."""
     inp = gen_random_mlp(N=16, D=4096, F=8 * 2048, T=8, dtype="bf16", act="gelu_tanh", bias=True,
                          seed=601, with_dy=False)
     g = to_gpu(inp)
