@@ -85,7 +85,13 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 5;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+    // Output staging for tensor stores: per epilogue warp two 4 KB buffers
+    // (one 32 x 32 chunk of fp32, or of bf16 C and bf16 Z), where the ring
+    // leaves room (not for 128-column tiles, whose 7th stage takes it).
+    static constexpr int OUT_BUF = 4096;
+    static constexpr int OUT_BYTES = 4 * 2 * OUT_BUF;
+    static constexpr bool TMA_OUT = SMEM_LIMIT - (1024 + STAGES * STAGE_BYTES + 256) >= OUT_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (TMA_OUT ? OUT_BYTES : 0) + 256;
     // barriers, then the TMEM address, the abort flag and the pair's load count
     static_assert(NUM_BARS * 8 + 12 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
@@ -101,6 +107,8 @@ struct TcParams {
     CUtensorMap tmA[kMaxG];
     CUtensorMap tmB[kMaxG];
     CUtensorMap tmB2[kMaxG];   // dual: the second B (up projection)
+    CUtensorMap tmC[kMaxG];    // tma_out: the output of each group (box 32 x 32)
+    CUtensorMap tmAux[kMaxG];  // tma_out, EPI_ACT with Z saved: Z of each group
     int M, N, K;
     int G, fold;
     int a_mn, b_mn;
@@ -125,6 +133,7 @@ struct TcParams {
     uint64_t timeout_ns;
     uint64_t drain_ns;   // limit of the waits for copies and MMAs already in flight
     int inject;          // failure-detection self test: the role that stalls (0: none)
+    int tma_out;         // 1: the epilogue writes C (and Z) through staging and tensor stores
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -265,11 +274,13 @@ __device__ __forceinline__ void dact_chunk(float (&v)[32], const float (&z)[32])
     for (int j = 0; j < 32; ++j) v[j] *= act_grad_bf16(ACT, z[j]);
 }
 
-// Epilogue of one thread: 32 consecutive columns [col0, col0 + 32) of output
-// row `row`, accumulator values in r[].
-__device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row, int col0, int M,
-                                               int N, const uint32_t (&r)[32]) {
-    float v[32];
+// Epilogue arithmetic of one thread, in two steps: 32 consecutive columns
+// [col0, col0 + 32) of output row `row`. epilogue_bias: v = acc (+ bias)
+// from the accumulator values in r[] (for EPI_ACT this is the pre-activation
+// Z); epilogue_act: v = act(v) (EPI_ACT) or v = v * act'(aux) (EPI_DACT).
+// Rows >= M (outside the output) read no auxiliary input.
+__device__ __forceinline__ void epilogue_bias(const EpiArgs& e, int g, int col0, int N,
+                                              const uint32_t (&r)[32], float (&v)[32]) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
     const bool full = (col0 + 32 <= N);
@@ -294,26 +305,12 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
                 if (col0 + j < N) v[j] += bf2f(b[j]);
         }
     }
-    if (row >= M) return;
+}
+
+__device__ __forceinline__ void epilogue_act(const EpiArgs& e, int g, int row, int col0, int M,
+                                             int N, float (&v)[32]) {
+    const bool full = (col0 + 32 <= N);
     if (e.kind == EPI_ACT) {
-        if (e.aux[g] != nullptr) {
-            __nv_bfloat16* z = static_cast<__nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w;
-                    w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-                    w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-                    w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-                    w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-                    reinterpret_cast<uint4*>(z)[q] = w;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (col0 + j < N) z[j] = __float2bfloat16_rn(v[j]);
-            }
-        }
         switch (e.act) {   // one dispatch per chunk, a tight loop per activation
             case TPMLP_ACT_RELU: act_chunk<TPMLP_ACT_RELU>(v); break;
             case TPMLP_ACT_GELU_ERF: act_chunk<TPMLP_ACT_GELU_ERF>(v); break;
@@ -321,21 +318,26 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
             default: act_chunk<TPMLP_ACT_GELU_TANH>(v); break;
         }
     } else if (e.kind == EPI_DACT) {
-        const __nv_bfloat16* z =
-            static_cast<const __nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
         float zv[32];
-        if (full) {
+        if (row >= M) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 w = *(reinterpret_cast<const uint4*>(z) + q);
-                unpack_bf16x2(w.x, zv[q * 8 + 0], zv[q * 8 + 1]);
-                unpack_bf16x2(w.y, zv[q * 8 + 2], zv[q * 8 + 3]);
-                unpack_bf16x2(w.z, zv[q * 8 + 4], zv[q * 8 + 5]);
-                unpack_bf16x2(w.w, zv[q * 8 + 6], zv[q * 8 + 7]);
-            }
+            for (int j = 0; j < 32; ++j) zv[j] = 0.f;
         } else {
+            const __nv_bfloat16* za =
+                static_cast<const __nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
+            if (full) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) zv[j] = col0 + j < N ? bf2f(z[j]) : 0.f;
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = *(reinterpret_cast<const uint4*>(za) + q);
+                    unpack_bf16x2(w.x, zv[q * 8 + 0], zv[q * 8 + 1]);
+                    unpack_bf16x2(w.y, zv[q * 8 + 2], zv[q * 8 + 3]);
+                    unpack_bf16x2(w.z, zv[q * 8 + 4], zv[q * 8 + 5]);
+                    unpack_bf16x2(w.w, zv[q * 8 + 6], zv[q * 8 + 7]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) zv[j] = col0 + j < N ? bf2f(za[j]) : 0.f;
+            }
         }
         switch (e.act) {
             case TPMLP_ACT_RELU: dact_chunk<TPMLP_ACT_RELU>(v, zv); break;
@@ -344,6 +346,42 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
             default: dact_chunk<TPMLP_ACT_GELU_TANH>(v, zv); break;
         }
     }
+}
+
+// 32 bf16 values of one row as four 16-byte words
+__device__ __forceinline__ void pack_row_bf16(const float (&v)[32], uint4 (&w)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        w[q].x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+        w[q].y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+        w[q].z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+        w[q].w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+    }
+}
+
+// Per-thread global stores of one row chunk (the form without staging):
+// Z (bf16, EPI_ACT with aux) and C (bf16 or fp32; by row blocks for the
+// reduce-scatter).
+__device__ __forceinline__ void store_z_thread(const EpiArgs& e, int g, int row, int col0, int M,
+                                               int N, const float (&z)[32]) {
+    if (row >= M) return;
+    __nv_bfloat16* za = static_cast<__nv_bfloat16*>(e.aux[g]) + (int64_t)row * e.ldaux + col0;
+    if (col0 + 32 <= N) {
+        uint4 w[4];
+        pack_row_bf16(z, w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(za)[q] = w[q];
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) za[j] = __float2bfloat16_rn(z[j]);
+    }
+}
+
+__device__ __forceinline__ void store_c_thread(const EpiArgs& e, int g, int row, int col0, int M,
+                                               int N, const float (&v)[32]) {
+    if (row >= M) return;
+    const bool full = (col0 + 32 <= N);
     int cg = g;
     int64_t crow = row;
     if (e.row_shard > 0) {          // reduce-scatter output: row block i -> C[i]
@@ -365,20 +403,37 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, int g, int row,
     } else {
         __nv_bfloat16* c = static_cast<__nv_bfloat16*>(e.C[cg]) + crow * e.ldc + col0;
         if (full) {
+            uint4 w[4];
+            pack_row_bf16(v, w);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 w;
-                w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-                w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-                w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-                w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-                reinterpret_cast<uint4*>(c)[q] = w;
-            }
+            for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(c)[q] = w[q];
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (col0 + j < N) c[j] = __float2bfloat16_rn(v[j]);
         }
+    }
+}
+
+// One row of a 32 x 32 output chunk into the warp's staging buffer, in the
+// layout of the output tensor map's swizzle: bf16 rows are 64 bytes with
+// 64-byte swizzle (16-byte word j of row r at word j ^ ((r >> 1) & 3)), fp32
+// rows 128 bytes with 128-byte swizzle (word j at j ^ (r & 7)), so the
+// warp's 16-byte stores of one word index hit distinct banks.
+__device__ __forceinline__ void stage_row(uint32_t buf, int r, bool f32, const float (&v)[32]) {
+    if (f32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(buf + (uint32_t)r * 128u + (uint32_t)((j ^ (r & 7)) << 4),
+                         __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    } else {
+        uint4 w[4];
+        pack_row_bf16(v, w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(buf + (uint32_t)r * 64u + (uint32_t)((j ^ ((r >> 1) & 3)) << 4), w[j].x,
+                         w[j].y, w[j].z, w[j].w);
     }
 }
 
@@ -430,7 +485,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    // staging for the epilogue's tensor stores (1024-byte aligned), then the barriers
+    const uint32_t sOut = sA0 + C::STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES +
+                                                 (C::TMA_OUT ? C::OUT_BYTES : 0));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // the odd CTA of a pair writes the number of loads it issued here (even CTA)
@@ -724,6 +782,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             if (lane == 0) live = wait_bounded(bar(STALL), 0, abort_flag, p.err, p.timeout_ns, true);
             live = __shfl_sync(0xffffffffu, live, 0);
         }
+        // Emits one 32-column chunk of the warp's 32 rows (`row` is this
+        // lane's, row0 the warp's first). With tensor stores the warp stages
+        // the chunk (C, and Z for EPI_ACT) in one of its two buffers and lane
+        // 0 writes it with one store per output; a buffer is written again
+        // once the stores issued from it two chunks earlier have read it.
+        uint32_t oset = 0;
+        const uint32_t obuf0 = sOut + (uint32_t)quarter * 2u * (uint32_t)C::OUT_BUF;
+        auto emit = [&](int g, int row, int row0, int col0, const uint32_t (&r)[32]) {
+            float v[32];
+            epilogue_bias(p.epi, g, col0, p.N, r, v);
+            const bool z_out = p.epi.kind == EPI_ACT && p.epi.aux[g] != nullptr;
+            if (C::TMA_OUT && p.tma_out) {
+                const uint32_t buf = obuf0 + oset * (uint32_t)C::OUT_BUF;
+                if (lane == 0) bulk_wait_read_all_but_one();
+                __syncwarp();
+                if (z_out) stage_row(buf + 2048u, lane, false, v);   // Z, before the activation
+                epilogue_act(p.epi, g, row, col0, p.M, p.N, v);
+                stage_row(buf, lane, p.epi.out_f32 != 0, v);
+                fence_proxy_async_smem();   // the staged rows, to the tensor-store proxy
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&p.tmC[g], buf, col0, row0);
+                    if (z_out) tma_store_2d(&p.tmAux[g], buf + 2048u, col0, row0);
+                    bulk_commit();
+                }
+                oset ^= 1u;
+            } else {
+                if (z_out) store_z_thread(p.epi, g, row, col0, p.M, p.N, v);
+                epilogue_act(p.epi, g, row, col0, p.M, p.N, v);
+                store_c_thread(p.epi, g, row, col0, p.M, p.N, v);
+            }
+        };
         for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); live && w.valid(); w.next()) {
             const int t = w.t;
             int g, m0, n0;
@@ -780,7 +870,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 }
                             }
                         }
-                        epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                        emit(g, row, row - lane, n0 + c, r);
                     }
                 } else if (xfer) {
                     int okf = 1;
@@ -905,7 +995,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             uint32_t r[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
-                            epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                            emit(g, row, row - lane, n0 + c, r);
                         }
                     }
                 }
@@ -916,7 +1006,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     __syncwarp();
                     tmem_ld_32cols(tbase + (uint32_t)c, r);
                     tmem_ld_wait();
-                    epilogue_chunk(p.epi, g, row, n0 + c, p.M, p.N, r);
+                    emit(g, row, row - lane, n0 + c, r);
                 }
             } else {
                 const int n0o = n0 / 2;
@@ -945,6 +1035,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 aph ^= 1u;
             }
         }
+        // every tensor store of this warp has completed (its staging buffers
+        // stay valid until then, and the outputs are written when the grid is)
+        if (C::TMA_OUT && p.tma_out && lane == 0) bulk_wait_all();
     }
 
     __syncwarp();
@@ -991,6 +1084,25 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Output map of the epilogue's tensor stores: `rows` x `cols` elements (bf16,
+// or fp32 with f32), row pitch ld elements, boxes of 32 x 32 with the swizzle
+// that matches the 64-byte (bf16) or 128-byte (fp32) staged rows.
+bool make_map_out(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                  bool f32) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int esz = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1199,6 +1311,19 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
         sk_cnt_bytes = (size_t)sh.sk_tiles * 4 * C::CTAS * sizeof(int);
     }
     kp.epi = pr.epi;
+    // the epilogue writes through staging and tensor stores where the tile
+    // configuration has room for the staging and every output has a map (not
+    // the gated epilogue, nor the reduce-scatter's row blocks)
+    kp.tma_out = 0;
+    if (C::TMA_OUT && !pr.dual && pr.epi.kind != EPI_SWIGLU && pr.epi.row_shard == 0) {
+        bool ok = true;
+        for (int g = 0; g < (pr.fold ? 1 : G) && ok; ++g) {
+            ok = make_map_out(&kp.tmC[g], pr.epi.C[g], pr.N, pr.M, pr.epi.ldc, pr.epi.out_f32 != 0);
+            if (ok && pr.epi.kind == EPI_ACT && pr.epi.aux[g] != nullptr)
+                ok = make_map_out(&kp.tmAux[g], pr.epi.aux[g], pr.N, pr.M, pr.epi.ldaux, false);
+        }
+        kp.tma_out = ok ? 1 : 0;
+    }
     kp.err = device_error_word();
     kp.timeout_ns = wait_timeout_ns();
     // copies and MMAs already issued complete in microseconds; their waits
