@@ -84,7 +84,7 @@ struct Cfg {
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 5;
+    static constexpr int NUM_BARS_BASE = 2 * STAGES + 2 * ACC_BUFS + 5;
     // Output staging for tensor stores: per epilogue warp two 4 KB buffers
     // (one 32 x 32 chunk of fp32, or of bf16 C and bf16 Z), where the ring
     // leaves room (not for 128-column tiles, whose 7th stage takes it).
@@ -92,6 +92,8 @@ struct Cfg {
     static constexpr int OUT_BYTES = 4 * 2 * OUT_BUF;
     static constexpr bool TMA_OUT = SMEM_LIMIT - (1024 + STAGES * STAGE_BYTES + 256) >= OUT_BYTES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (TMA_OUT ? OUT_BYTES : 0) + 256;
+    // with staging, two barriers per epilogue warp for the act' epilogue's Z loads
+    static constexpr int NUM_BARS = NUM_BARS_BASE + (TMA_OUT ? 8 : 0);
     // barriers, then the TMEM address, the abort flag and the pair's load count
     static_assert(NUM_BARS * 8 + 12 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
@@ -415,6 +417,33 @@ __device__ __forceinline__ void store_c_thread(const EpiArgs& e, int g, int row,
     }
 }
 
+// Row r of a 32 x 32 bf16 chunk loaded by a tensor load into a 64-byte
+// swizzled buffer (the layout stage_row writes), as 32 floats.
+__device__ __forceinline__ void load_row_bf16_smem(uint32_t buf, int r, float (&z)[32]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(buf + (uint32_t)r * 64u + (uint32_t)((j ^ ((r >> 1) & 3)) << 4))
+                     : "memory");
+        unpack_bf16x2(w0, z[j * 8 + 0], z[j * 8 + 1]);
+        unpack_bf16x2(w1, z[j * 8 + 2], z[j * 8 + 3]);
+        unpack_bf16x2(w2, z[j * 8 + 4], z[j * 8 + 5]);
+        unpack_bf16x2(w3, z[j * 8 + 6], z[j * 8 + 7]);
+    }
+}
+
+// v *= act'(z) over one chunk
+__device__ __forceinline__ void dact_apply(int act, float (&v)[32], const float (&z)[32]) {
+    switch (act) {
+        case TPMLP_ACT_RELU: dact_chunk<TPMLP_ACT_RELU>(v, z); break;
+        case TPMLP_ACT_GELU_ERF: dact_chunk<TPMLP_ACT_GELU_ERF>(v, z); break;
+        case TPMLP_ACT_GELU_SIGMOID: dact_chunk<TPMLP_ACT_GELU_SIGMOID>(v, z); break;
+        default: dact_chunk<TPMLP_ACT_GELU_TANH>(v, z); break;
+    }
+}
+
 // One row of a 32 x 32 output chunk into the warp's staging buffer, in the
 // layout of the output tensor map's swizzle: bf16 rows are 64 bytes with
 // 64-byte swizzle (16-byte word j of row r at word j ^ ((r >> 1) & 3)), fp32
@@ -498,7 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // it), XCNT carries the odd CTA's load count to the even CTA
     const int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = TFULL + ACC_BUFS,
               DRAIN = TEMPTY + ACC_BUFS, RFREE = DRAIN + 1, RFULL = DRAIN + 2, STALL = DRAIN + 3,
-              XCNT = DRAIN + 4;
+              XCNT = DRAIN + 4, ZLD = DRAIN + 5;   // ZLD + 2 * quarter + set: Z chunk loads
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -529,6 +558,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         mbar_init(bar(RFULL), ks > 1 ? (ks - 1) * red_warps * 32 : 1);   // every peer lane
         mbar_init(bar(STALL), 1);
         mbar_init(bar(XCNT), 1);
+        if constexpr (C::TMA_OUT)
+            for (int z = 0; z < 8; ++z) mbar_init(bar(ZLD + z), 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -789,16 +820,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         // once the stores issued from it two chunks earlier have read it.
         uint32_t oset = 0;
         const uint32_t obuf0 = sOut + (uint32_t)quarter * 2u * (uint32_t)C::OUT_BUF;
-        auto emit = [&](int g, int row, int row0, int col0, const uint32_t (&r)[32]) {
+        // act' epilogue with staging: each chunk's Z arrives by a tensor load
+        // into the Z half of the chunk's staging set (issued one chunk ahead,
+        // or at the start of a tile before its accumulator is ready), on one
+        // of the warp's two barriers; zpend / zph hold each set's pending
+        // load and barrier phase
+        const bool zin = C::TMA_OUT && p.tma_out && p.epi.kind == EPI_DACT;
+        uint32_t zpend = 0, zph = 0;
+        auto zbar = [&](uint32_t set) { return bar(ZLD + 2 * quarter + (int)set); };
+        auto zload = [&](uint32_t set, int g, int col0, int row0) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(zbar(set), 2048u);
+                tma_load_2d(obuf0 + set * (uint32_t)C::OUT_BUF + 2048u, &p.tmAux[g], zbar(set), col0, row0);
+            }
+            zpend |= 1u << set;
+        };
+        // next_col0: the next chunk this warp emits for the same rows, or -1
+        auto emit = [&](int g, int row, int row0, int col0, const uint32_t (&r)[32], int next_col0) {
             float v[32];
             epilogue_bias(p.epi, g, col0, p.N, r, v);
             const bool z_out = p.epi.kind == EPI_ACT && p.epi.aux[g] != nullptr;
             if (C::TMA_OUT && p.tma_out) {
                 const uint32_t buf = obuf0 + oset * (uint32_t)C::OUT_BUF;
+                if (zin) {
+                    if (!((zpend >> oset) & 1u)) zload(oset, g, col0, row0);
+                    if (next_col0 >= 0) zload(oset ^ 1u, g, next_col0, row0);
+                }
                 if (lane == 0) bulk_wait_read_all_but_one();
                 __syncwarp();
                 if (z_out) stage_row(buf + 2048u, lane, false, v);   // Z, before the activation
-                epilogue_act(p.epi, g, row, col0, p.M, p.N, v);
+                if (zin) {
+                    const uint32_t par = (zph >> oset) & 1u;
+                    int okz = 1;
+                    if (lane == 0) okz = wait_fast(zbar(oset), par, abort_flag, p.err, p.timeout_ns, true);
+                    okz = __shfl_sync(0xffffffffu, okz, 0);
+                    if (okz) {
+                        mbar_try_wait(zbar(oset), par);   // each lane acquires the completed load
+                        zpend &= ~(1u << oset);
+                        zph ^= 1u << oset;
+                    }
+                    float zv[32];
+                    load_row_bf16_smem(buf + 2048u, lane, zv);
+                    dact_apply(p.epi.act, v, zv);
+                } else {
+                    epilogue_act(p.epi, g, row, col0, p.M, p.N, v);
+                }
                 stage_row(buf, lane, p.epi.out_f32 != 0, v);
                 fence_proxy_async_smem();   // the staged rows, to the tensor-store proxy
                 __syncwarp();
@@ -814,10 +880,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 store_c_thread(p.epi, g, row, col0, p.M, p.N, v);
             }
         };
+        // the next chunk a warp emits after column c of a tile starting at n0
+        auto next_of = [&](int n0, int c) { return (c + 32 < BN && n0 + c + 32 < p.N) ? n0 + c + 32 : -1; };
         for (Work w(p, first_tile, tile_step, kb_lo, kb_hi, kb_total); live && w.valid(); w.next()) {
             const int t = w.t;
             int g, m0, n0;
             decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
+            // act' epilogue: the tile's first Z chunk loads while the accumulator fills
+            if (zin && !w.partial() && !p.dual && ks == 1 && !((zpend >> oset) & 1u))
+                zload(oset, g, n0, m0 + (int)rank * BM + quarter * 32);
             // one lane waits; the warp stays converged for the .sync.aligned TMEM loads
             int ok = 1;
             // (sleeping 1 us between polls: 0.4-1.4% fewer cycles for the GEMM)
@@ -870,7 +941,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 }
                             }
                         }
-                        emit(g, row, row - lane, n0 + c, r);
+                        emit(g, row, row - lane, n0 + c, r, next_of(n0, c));
                     }
                 } else if (xfer) {
                     int okf = 1;
@@ -995,7 +1066,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             uint32_t r[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
-                            emit(g, row, row - lane, n0 + c, r);
+                            emit(g, row, row - lane, n0 + c, r, next_of(n0, c));
                         }
                     }
                 }
@@ -1006,7 +1077,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     __syncwarp();
                     tmem_ld_32cols(tbase + (uint32_t)c, r);
                     tmem_ld_wait();
-                    emit(g, row, row - lane, n0 + c, r);
+                    emit(g, row, row - lane, n0 + c, r, next_of(n0, c));
                 }
             } else {
                 const int n0o = n0 / 2;
@@ -1036,8 +1107,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             }
         }
         // every tensor store of this warp has completed (its staging buffers
-        // stay valid until then, and the outputs are written when the grid is)
-        if (C::TMA_OUT && p.tma_out && lane == 0) bulk_wait_all();
+        // stay valid until then, and the outputs are written when the grid is),
+        // and no Z load this warp issued is still in flight
+        if (C::TMA_OUT && p.tma_out && lane == 0) {
+            bulk_wait_all();
+            for (uint32_t set = 0; set < 2; ++set)
+                if ((zpend >> set) & 1u)
+                    wait_bounded(zbar(set), (zph >> set) & 1u, abort_flag, p.err, p.drain_ns, false);
+        }
     }
 
     __syncwarp();
@@ -1319,7 +1396,7 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
         bool ok = true;
         for (int g = 0; g < (pr.fold ? 1 : G) && ok; ++g) {
             ok = make_map_out(&kp.tmC[g], pr.epi.C[g], pr.N, pr.M, pr.epi.ldc, pr.epi.out_f32 != 0);
-            if (ok && pr.epi.kind == EPI_ACT && pr.epi.aux[g] != nullptr)
+            if (ok && (pr.epi.kind == EPI_ACT || pr.epi.kind == EPI_DACT) && pr.epi.aux[g] != nullptr)
                 ok = make_map_out(&kp.tmAux[g], pr.epi.aux[g], pr.N, pr.M, pr.epi.ldaux, false);
         }
         kp.tma_out = ok ? 1 : 0;
