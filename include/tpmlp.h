@@ -324,7 +324,7 @@ tpmlp_status tpmlp_selftest_gemm_stall(int role);
  * all G groups into one output (the split-K shard sum), dual = 1 for the
  * gated GEMM (N counts outputs), balanced = 1 when the call's workspace holds
  * the few-token scratch (tpmlp_workspace_bytes_balanced). Writes the tile's
- * accumulator columns (128 or 256), the CTAs that issue one MMA (1, or 2 for
+ * accumulator columns (128, 192 or 256), the CTAs that issue one MMA (1, or 2 for
  * a CTA pair) and the K split: the CTAs of a cluster that share one tile's
  * K range (1 = no split; 2-4 for folded GEMMs with M <= 64, where the weights
  * stream from HBM and the tiles are fewer than the SMs), or 0 for the

@@ -16,7 +16,8 @@
 // Four launch forms, chosen per GEMM by run_gemm_tc:
 //   - CTA pair (cluster of 2, M > 128): cta_group::2 MMAs of M = 256; each
 //     CTA stages its own 128 A rows and half of the B rows;
-//   - single CTA, 128 x 256 or 128 x 128 tiles;
+//   - single CTA, 128 x 256 or 128 x 128 tiles (and 128 x 192 for GEMMs that
+//     stream weights for a few token rows);
 //   - K split (folded GEMMs with M <= 64): a cluster of 2-4 CTAs shares one
 //     tile's k-blocks; the peers send their partial accumulator rows to the
 //     leader's freed stage memory over DSMEM and the leader adds them before
@@ -83,7 +84,8 @@ struct Cfg {
     static constexpr int SMEM_LIMIT = 232448;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    // two accumulators of BN columns, allocated as a power of two
+    static constexpr int TMEM_COLS = ACC_BUFS * BN <= 256 ? 256 : 512;
     static constexpr int NUM_BARS_BASE = 2 * STAGES + 2 * ACC_BUFS + 5;
     // Output staging for tensor stores: per epilogue warp two 4 KB buffers
     // (one 32 x 32 chunk of fp32, or of bf16 C and bf16 Z), where the ring
@@ -1483,10 +1485,14 @@ Plan choose_plan(const GemmProblem& pr) {
         double rate;
     };
     // ks = 0: stream-K (with the scratch)
+    // 192-column tiles only stream weights (M <= 64): 64 of them cover the
+    // N = 12288 row GEMM, which a 2-CTA K split then runs on 128 SMs
     const Cand cands[] = {{256, true, 1, 1.08}, {256, false, 1, 1.0}, {128, false, 1, 0.85},
                           {256, true, 0, 1.08},  {256, false, 0, 1.0},  {128, false, 0, 0.85},
                           {256, false, 2, 1.0},  {256, false, 3, 1.0}, {256, false, 4, 1.0},
-                          {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85}};
+                          {128, false, 2, 0.85}, {128, false, 3, 0.85}, {128, false, 4, 0.85},
+                          {192, false, 1, 0.95}, {192, false, 0, 0.95}, {192, false, 2, 0.95},
+                          {192, false, 3, 0.95}, {192, false, 4, 0.95}};
     const int ncand = (int)(sizeof(cands) / sizeof(cands[0]));
     const int groups = pr.fold ? 1 : pr.G;
     const int64_t kb_total = (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + BKB - 1) / BKB);
@@ -1501,6 +1507,7 @@ Plan choose_plan(const GemmProblem& pr) {
     for (int i = 0; i < ncand; ++i) {
         const Cand& c = cands[i];
         if (c.pair && pr.M <= 128) continue;   // a pair covers 256 rows
+        if (c.bn == 192 && (pr.M > KSPLIT_ROWS || pr.dual)) continue;
         if (c.ks > 1 && (!pr.fold || pr.M > KSPLIT_ROWS || pr.dual || c.ks > kb_total)) continue;
         const int64_t tile_m = c.pair ? 256 : 128;
         const int64_t n_out = pr.dual ? c.bn / 2 : c.bn;   // outputs per tile along N
@@ -1508,7 +1515,7 @@ Plan choose_plan(const GemmProblem& pr) {
                               ((pr.N + n_out - 1) / n_out);
         // one CTA's streaming rate with BN-column tiles, and the weight bytes
         // of a tile (all its k-blocks of BN columns, both halves if dual)
-        const double r_cta = c.bn == 128 ? 54e9 : 66e9;
+        const double r_cta = c.bn == 128 ? 54e9 : c.bn == 192 ? 60e9 : 66e9;
         const double tile_bytes = (double)c.bn * (double)kb_total * BKB * 2.0;
         auto wave = [&](double ctas, double bytes) {
             const double hbm = ctas * bytes / kHbm, one = bytes / r_cta;
@@ -1520,8 +1527,9 @@ Plan choose_plan(const GemmProblem& pr) {
             const int64_t kbt = c.pair ? (int64_t)(pr.fold ? pr.G : 1) * ((pr.K + 2 * BKB - 1) / (2 * BKB))
                                        : kb_total;
             const SkShape sh = c.pair ? sk_shape<256, true>(pr, tiles, kbt)
-                                      : c.bn == 128 ? sk_shape<128, false>(pr, tiles, kbt)
-                                                    : sk_shape<256, false>(pr, tiles, kbt);
+                               : c.bn == 128 ? sk_shape<128, false>(pr, tiles, kbt)
+                               : c.bn == 192 ? sk_shape<192, false>(pr, tiles, kbt)
+                                             : sk_shape<256, false>(pr, tiles, kbt);
             if (!sh.ok) continue;
             if (pr.M > KSPLIT_ROWS) {
                 // full waves, then one K chunk of a part-wave tile per unit
@@ -1536,6 +1544,7 @@ Plan choose_plan(const GemmProblem& pr) {
         } else {
             int64_t units = 0;
             if (c.bn == 128) units = resident_units<128, false>(c.ks);
+            else if (c.bn == 192) units = resident_units<192, false>(c.ks);
             else if (c.pair) units = resident_units<256, true>(2);
             else units = resident_units<256, false>(c.ks);
             if (units < 1) continue;
@@ -1577,6 +1586,7 @@ tpmlp_status run_gemm_tc(const GemmProblem& pr, cudaStream_t s) {
     const Plan c = choose_plan(pr);
     if (!c.ok) return TPMLP_ERR_CUDA;
     if (c.bn == 128) return launch<128, false>(pr, s, c.ks);
+    if (c.bn == 192) return launch<192, false>(pr, s, c.ks);
     if (c.pair) return launch<256, true>(pr, s, c.ks);
     return launch<256, false>(pr, s, c.ks);
 }

@@ -44,13 +44,16 @@ def col_plan(N, D, T, balanced=True):
 
 def test_plans_take_stream_k_only_with_the_scratch_and_few_rows():
     # the weight-streaming forward of N=16, D=12288, F=49152, T=8 (measured):
-    # whole 128-column tiles for the column GEMM (2.5 waves, started together
-    # on the same weight rows), a K split over 2-CTA clusters of 256-column
-    # tiles for the folded row GEMM (96 CTAs in two lockstep fronts), whole
-    # 256-column tiles for the grouped partial-sum GEMM; stream-K for none
-    assert tp.tpmlp_gemm_plan(16, 6144, 12288, 8, balanced=True) == (128, 1, 1)
-    assert tp.tpmlp_gemm_plan(16, 12288, 6144, 8, fold=True, balanced=True) == (256, 1, 2)
+    # whole 192-column tiles for the column GEMM (256 tiles, 1.7 waves, started
+    # together on the same weight rows), a K split over 2-CTA clusters of
+    # 192-column tiles for the folded row GEMM (128 CTAs in two lockstep
+    # fronts), whole 256-column tiles for the grouped partial-sum GEMM;
+    # stream-K for none
+    assert tp.tpmlp_gemm_plan(16, 6144, 12288, 8, balanced=True) == (192, 1, 1)
+    assert tp.tpmlp_gemm_plan(16, 12288, 6144, 8, fold=True, balanced=True) == (192, 1, 2)
     assert tp.tpmlp_gemm_plan(16, 12288, 6144, 8, balanced=True) == (256, 1, 1)
+    # 192-column tiles only for a few token rows
+    assert tp.tpmlp_gemm_plan(65, 12288, 6144, 8, fold=True)[0] != 192
     # a few tiles of a small block take it (the shapes below)
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=True)[2] == 0
     assert tp.tpmlp_gemm_plan(16, FS, 1024, 2, balanced=False)[2] != 0
