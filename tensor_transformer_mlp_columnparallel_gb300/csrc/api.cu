@@ -74,6 +74,16 @@ bool pdl_enabled() {
     return on;
 }
 
+bool alternate_orders() {
+    // TPMLP_ALT_ORDER=0 in the environment keeps every GEMM's tiles and K
+    // loops in plain ascending order (for A/B timing and traffic counts)
+    static const bool on = [] {
+        const char* v = getenv("TPMLP_ALT_ORDER");
+        return v == nullptr || strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
 int device_sm_count() {
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return 1;

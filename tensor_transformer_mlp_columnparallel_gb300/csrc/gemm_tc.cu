@@ -57,7 +57,7 @@ constexpr int UMMA_K = 16;        // K of one kind::f16 MMA
 constexpr int NUM_THREADS = 192;
 constexpr int ACC_BUFS = 2;
 constexpr int BOX_MN = 64;        // MN extent of an MN-major box (128 bytes)
-constexpr int GROUP_M = 8;        // raster band height, in M tiles
+constexpr int GROUP_M = 12;       // raster band height, in M tiles
 constexpr int KSPLIT_ROWS = 64;   // rows a K-split cluster exchanges (M <= 64)
 
 // BN: accumulator columns (MMA N). PAIR: a CTA pair (cluster of 2) issues
@@ -138,6 +138,8 @@ struct TcParams {
     uint64_t drain_ns;   // limit of the waits for copies and MMAs already in flight
     int inject;          // failure-detection self test: the role that stalls (0: none)
     int tma_out;         // 1: the epilogue writes C (and Z) through staging and tensor stores
+    int alt;             // bit 0: whole tiles of odd waves walk their K range from the top
+                         // down; bit 1: odd bands walk their tiles in reverse (decode_tile)
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -169,6 +171,9 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_
 //             A panel is read from HBM once for all groups;
 //   raster 2: B is the same matrix for every group: the same with the roles
 //             of M and N swapped.
+// With p.alt bit 1, odd bands walk their tiles in reverse, so the wave that
+// crosses from one band to the next works on the same B (raster 2: A) panels
+// on both sides of the boundary.
 template <int BN, int TILE_M>
 __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& m0, int& n0) {
     int mt, nt;
@@ -182,13 +187,15 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
         const int in_band = local - band * p.band * p.n_tiles;
         mt = first_m + in_band % band_m;
         nt = in_band / band_m;
+        if ((p.alt & 2) && (band & 1)) nt = p.n_tiles - 1 - nt;
     } else if (p.raster == 1) {
         const int band = t / (p.band * p.n_tiles * p.G);
         const int first_m = band * p.band;
         const int band_m = min(p.m_tiles - first_m, p.band);
         const int in_band = t - band * p.band * p.n_tiles * p.G;
         mt = first_m + in_band % band_m;
-        const int rest = in_band / band_m;
+        int rest = in_band / band_m;
+        if ((p.alt & 2) && (band & 1)) rest = p.n_tiles * p.G - 1 - rest;
         g = rest / p.n_tiles;
         nt = rest - g * p.n_tiles;
     } else {
@@ -197,7 +204,8 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
         const int band_n = min(p.n_tiles - first_n, p.band);
         const int in_band = t - band * p.band * p.m_tiles * p.G;
         nt = first_n + in_band % band_n;
-        const int rest = in_band / band_n;
+        int rest = in_band / band_n;
+        if ((p.alt & 2) && (band & 1)) rest = p.m_tiles * p.G - 1 - rest;
         g = rest / p.m_tiles;
         mt = rest - g * p.m_tiles;
     }
@@ -673,14 +681,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 decode_tile<BN, C::TILE_M>(p, t, g, m0, n0);
                 const int am0 = m0 + (int)rank * BM;          // this CTA's A rows
                 const int bn0 = n0 + (int)rank * C::B_ROWS;   // this CTA's B rows (N)
+                // Whole tiles of every other wave (the CTA's tiles t, t + step,
+                // ... are one per wave) take their k-blocks from the last down:
+                // such a wave starts on the K slices of the panels it shares with
+                // the wave before, which that wave read last and which are the
+                // likeliest to be still in L2. The MMA issuer counts k-blocks
+                // only, so the order is the producer's alone.
+                const bool down = (p.alt & 1) && !w.sk && ((w.t / w.step) & 1);
+                const int kb_first = down ? w.kb1 - 1 : w.kb0;
                 // shard of the first k-block and its K offset inside the shard
-                int gk = p.fold ? w.kb0 / kb_per_group : g;
-                int k0 = (p.fold ? w.kb0 - (w.kb0 / kb_per_group) * kb_per_group : w.kb0) * C::BK;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, k0 += C::BK) {
-                    if (k0 == k_group) {   // folded K loop: next shard
-                        k0 = 0;
-                        ++gk;
-                    }
+                int gk = p.fold ? kb_first / kb_per_group : g;
+                int k0 = (p.fold ? kb_first - (kb_first / kb_per_group) * kb_per_group : kb_first) * C::BK;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_fast(bar(EMPTY + s), ph ^ 1u, abort_flag, p.err, p.timeout_ns, true)) {
                         ok = false;
                         break;
@@ -691,6 +703,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     if (++s == C::STAGES) {
                         s = 0;
                         ph ^= 1u;
+                    }
+                    // next k-block's shard and offset (folded K: shards in turn)
+                    if (down) {
+                        k0 -= C::BK;
+                        if (k0 < 0) {
+                            k0 = k_group - C::BK;
+                            --gk;
+                        }
+                    } else {
+                        k0 += C::BK;
+                        if (k0 == k_group) {
+                            k0 = 0;
+                            ++gk;
+                        }
                     }
                 }
             }
@@ -1363,8 +1389,9 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
             shared_a = shared_a && pr.A[g] == pr.A[0];
             shared_b = shared_b && pr.B[g] == pr.B[0];
         }
-        // bands of 8 tiles: a sweep of 2..32 on the fwd+bwd workload gave the
-        // least HBM traffic at 8 (time differed by under 2%)
+        // bands of 12 tiles: with the alternating orders a sweep of 4..24 on
+        // the fwd+bwd GEMMs read the least from DRAM at 12 (the folded ones
+        // 9% less than at 8, the rest equal) and ran the step as fast as any
         kp.raster = shared_a ? 1 : (shared_b ? 2 : 0);
         kp.band = GROUP_M;
     }
@@ -1390,6 +1417,9 @@ tpmlp_status launch(const GemmProblem& pr, cudaStream_t s, int ks = 1) {
         sk_cnt_bytes = (size_t)sh.sk_tiles * 4 * C::CTAS * sizeof(int);
     }
     kp.epi = pr.epi;
+    // alternating orders for the tiles of more than one wave; the few-token
+    // forms stream each operand once and keep the plain order
+    kp.alt = pr.M > KSPLIT_ROWS && alternate_orders() ? 3 : 0;
     // the epilogue writes through staging and tensor stores where the tile
     // configuration has room for the staging and every output has a map (not
     // the gated epilogue, nor the reduce-scatter's row blocks)

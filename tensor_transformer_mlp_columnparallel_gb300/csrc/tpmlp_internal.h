@@ -104,6 +104,7 @@ int* device_error_word();          // per current device; NULL on failure
 uint64_t wait_timeout_ns();
 int gemm_stall_role();             // failure-detection self test of the GEMM (0: off)
 bool pdl_enabled();                // programmatic dependent launch (TPMLP_PDL != 0)
+bool alternate_orders();           // odd waves walk K down, odd bands their tiles back (TPMLP_ALT_ORDER != 0)
 int device_sm_count();
 
 // Counts the launch and, when timing is on, brackets it with CUDA events

@@ -14,7 +14,11 @@ Each case first checks its own premise (magnitudes within 256) on the oracle.
 
 Forms, asked of the library's own plan where the choice depends on the device:
 - CTA pair with 128-deep K stages (more than 128 token rows), ragged in every
-  dimension, reduction lengths 4104-4160;
+  dimension, reduction lengths 4104-4160, over several waves and bands of
+  tiles: whole tiles of odd waves take their k-blocks from the last down
+  (across the shard boundary of a folded K) and odd bands walk their tiles
+  in reverse; the same block again with the plain ascending orders
+  (TPMLP_ALT_ORDER=0, in a fresh process);
 - single-CTA 128-row tiles (65-128 token rows, 64-deep stages);
 - the cluster K split of 2, 3 and 4 CTAs (at most 64 token rows, no scratch);
 - stream-K (at most 64 token rows, with the scratch), and the part-wave
@@ -22,6 +26,10 @@ Forms, asked of the library's own plan where the choice depends on the device:
   full waves, the last wave's k-blocks dealt out);
 - the fp32 GEMM's cluster K split (up to 8 CTAs per tile).
 """
+
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -132,10 +140,28 @@ def test_cta_pair_128_deep_ring_long_k_ragged():
     than 4096 deep, in 128-deep stages of a 3-stage ring."""
     T = 2
     N, D, Fs = pair_shape(T)
+    # premise: more than two waves of pair tiles and more than one band of
+    # 12 tile rows in the column GEMM and the folded row GEMM
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    m_tiles = -(-N // 256)
+    for n_tiles in (T * -(-Fs // 256), -(-D // 256)):
+        assert m_tiles * n_tiles > 2 * pairs and m_tiles > 12
     inp = gen_sparse_integer_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", seed=301)
     f, g = expected(inp, bias_grads=False)
     for mode in MODES:
         assert_exact(inp, run_block(inp, mode, True, False), f, g, f"pair {mode}")
+
+
+def test_cta_pair_plain_orders_bit_exact():
+    """The CTA-pair case with every tile's K loop ascending and every band
+    walked forwards (the library reads TPMLP_ALT_ORDER once per process)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, TPMLP_ALT_ORDER="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.abspath(__file__), "-q",
+                        "-p", "no:cacheprovider", "-m", "gpu",
+                        "-k", "test_cta_pair_128_deep_ring_long_k_ragged"],
+                       env=env, cwd=root, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and "1 passed" in r.stdout, r.stdout[-3000:] + r.stderr[-2000:]
 
 
 def test_single_cta_tiles_long_k_with_biases():
