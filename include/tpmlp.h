@@ -42,6 +42,14 @@
  * - bf16 path alignment: every pointer 16-byte aligned and D % 8 == 0,
  *   (F/T) % 8 == 0 (tensor-memory-access row pitches are multiples of 16
  *   bytes); otherwise TPMLP_ERR_ALIGN.
+ * - Two environment variables, read once per process, change how kernels are
+ *   launched, never what they compute (results stay within the same
+ *   tolerances; integer-valued inputs give the same bits):
+ *   TPMLP_PDL=0 launches every kernel fully serialised after the previous
+ *   one on its stream (default: programmatic dependent launch);
+ *   TPMLP_ALT_ORDER=0 keeps every GEMM tile's K loop ascending and every band
+ *   of tiles in one direction (default: odd waves walk K downwards and odd
+ *   bands walk their tiles back, for L2 reuse).
  */
 #ifndef TPMLP_H
 #define TPMLP_H
