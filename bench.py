@@ -724,7 +724,7 @@ def cublas_same_shapes(blk, steps, warmup, stream):
     return 6 * 2.0 * N * D * F / (cub_ms * 1e-3) / 1e12, cub_ms / ours_ms, ratio
 
 
-def e2e_measure(blk, steps, stream, regions=1, depth=4):
+def e2e_measure(blk, steps, stream, regions=1, depth=4, warmup=5, idle_s=2.0):
     """The same step through the public API with host buffers. Every step
     copies that step's batch (X, dY) from pinned host memory to the device and
     its activation results (Y, dX) back to pinned host memory; the weights and
@@ -797,12 +797,16 @@ def e2e_measure(blk, steps, stream, regions=1, depth=4):
         stream.wait_stream(cin)
         stream.wait_stream(cout)
 
-    run(depth)
+    # Like the device-timed region, the first region starts from an idle GPU
+    # after `warmup` steps through this same loop; `regions` timed regions of
+    # `steps` steps each follow back to back. The host link now and then holds
+    # a few 268 MB copies for 10-45 ms each instead of 1.3-1.6 ms (also with no
+    # kernel running; compute spans stay the same); the prefetch depth hides
+    # most of that, the median region is the figure, all are reported.
     torch.cuda.synchronize()
-    # `regions` timed regions of `steps` steps each. The host link now and then
-    # holds a few 268 MB copies for 18-29 ms each instead of 1.3-1.6 ms (the
-    # copy engine, not the kernels: compute spans stay the same); the prefetch
-    # depth hides most of that, the median region is the figure, all are reported.
+    time.sleep(idle_s)
+    run(max(warmup, 1))
+    torch.cuda.synchronize()
     region_ms = []
     for _ in range(regions):
         spans.clear()
@@ -890,16 +894,12 @@ def run_ours(args):
         n_e = args.steps
         # the device-timed region started from an idle GPU after a few warm-up
         # steps; under the power cap the clock then drifts down with sustained
-        # load, so the end-to-end region starts from the same state (the GPU
-        # idles briefly first) and its clocks are sampled as well
-        torch.cuda.synchronize()
-        time.sleep(2.0)
-        for _ in range(args.warmup):
-            blk.step()
-        torch.cuda.synchronize()
+        # load, so each end-to-end region starts from the same state (see
+        # e2e_measure) and their clocks are sampled as well
         eclk = ClockSampler(local)
         eclk.start()
-        e_regions, h2d, d2h, e_compute = e2e_measure(blk, n_e, stream, regions=3)
+        e_regions, h2d, d2h, e_compute = e2e_measure(blk, n_e, stream, regions=3,
+                                                     warmup=args.warmup)
         eclk = eclk.stop()
         e_ms = float(np.median(e_regions))
         line["e2e"] = {"value": flops_step * n_e / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
