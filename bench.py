@@ -77,6 +77,9 @@ def parse(argv=None):
                          "tokens (small cases for profiling)")
     ap.add_argument("--only-decode", action="store_true",
                     help="time only the weight-streaming forward (N=16 D=12288 F=49152 T=8)")
+    ap.add_argument("--only-f32", action="store_true",
+                    help="time only the exact-fp32 block (N=64 D=256 F=1024 T=2, ReLU, biases), "
+                         "forward and forward + backward")
     return ap.parse_args(argv)
 
 
@@ -1002,6 +1005,14 @@ def run_only(args):
                "results": measure_ce(dev, stream, iters, pk, args.only_ce)}
     elif args.only_embedding:
         res = {"only": "vocab_embedding", "results": measure_embedding(dev, iters, pk)}
+    elif args.only_f32:
+        import tensor_transformer_mlp_columnparallel_gb300 as tp
+        fb = Block(MLP_CONFIGS["mlp_f32_relu_n64_d256_f1024_t2"], args.mode, dev)
+        res = {"only": "f32_block", "mode": args.mode, "results": {}, "kernels": {}}
+        for label, fn in (("fwd", fb.forward), ("fwdbwd", fb.step)):
+            ms, _, t = _lib_timed(tp, fn, iters, stream)
+            res["results"][f"{label}_us"] = rnd(ms * 1e3)
+            res["kernels"][label] = kernel_table(t, ms * iters)
     else:
         import tensor_transformer_mlp_columnparallel_gb300 as tp
         fc = MLP_CONFIGS["mlp_bf16_gelu_n16_d12288_f49152_t8"]
@@ -1015,7 +1026,7 @@ def run_only(args):
 
 def main():
     args = parse()
-    if args.only_ce or args.only_embedding or args.only_decode:
+    if args.only_ce or args.only_embedding or args.only_decode or args.only_f32:
         run_only(args)
         return
     if args.impl == "reference":
