@@ -56,6 +56,7 @@ BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0,
            "source": "GB300 datasheet: 2.25 PFLOP/s dense bf16, HBM3e 7.9 TB/s"}
 BURST_REGION_S = 2.0   # timed regions shorter than this are held to the burst bf16 peak
+DATA = "synthetic (seeded; X, dY ~ N(0,1), W ~ N(0,0.02))"
 
 
 def parse(argv=None):
@@ -226,6 +227,17 @@ class Block:
                          self.cfg.act, self.mode, self.ws)
         tp.tpmlp_backward(self.X, self.W1, self.W2, self.H, self.Z, self.dY, self.dX, self.dW1,
                           self.dW2, None, None, self.cfg.act, self.mode, self.ws)
+
+
+def line_config(cfg, mode, world):
+    """The JSON line's `config`: the workload, the same for both arms (the
+    reference arm computes the same products on a sample of its tokens, which
+    its `cpu_baseline.sample` states)."""
+    return {"workload": cfg.name, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
+            "F": cfg.F, "T": cfg.T, "act": cfg.act, "bias": False,
+            "reduce_mode": mode, "pass": "forward+backward",
+            "l2": "inputs larger than L2 (weights 0.94 GB, activations 1.1 GB per step)",
+            "parallelism": f"replicas x{world} (T logical shards per GPU)"}
 
 
 def workload_config(args):
@@ -881,12 +893,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "ms_per_step_median": float(np.median(per_step)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; X, dY ~ N(0,1), W ~ N(0,0.02))",
-        "config": {"workload": cfg.name, "N": cfg.N, "B": cfg.B, "L": cfg.L, "D": cfg.D,
-                   "F": cfg.F, "T": cfg.T, "act": cfg.act, "bias": False,
-                   "reduce_mode": args.mode, "pass": "forward+backward",
-                   "l2": "inputs larger than L2 (weights 0.94 GB, activations 1.1 GB per step)",
-                   "parallelism": f"replicas x{world} (T logical shards per GPU)"},
+        "data": DATA,
+        "config": line_config(cfg, args.mode, world),
         "frac_of_peak_step": value / world / peak,
         "roofline": roof,
         "gpu_launches": launches,
@@ -955,7 +963,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    cfg = MLP_CONFIGS[WORKLOAD]
+    cfg = workload_config(args)
     tokens = 32
     inp = gen_mlp_inputs(cfg, N=tokens)
     W1 = oracle.mlp.as_f64(inp.W1)
@@ -979,9 +987,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": cfg.name, "N": cfg.N, "D": cfg.D, "F": cfg.F, "T": cfg.T,
-                   "act": cfg.act, "pass": "forward+backward"},
+        "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": line_config(cfg, args.mode, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
