@@ -959,30 +959,38 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
+    """The reference arm: the float64 oracle as it stands, on the host cores,
+    timed over --steps steps after --warmup, each step a bounded sample of the
+    workload: the fwd+bwd of shard 0 of T (W1[:, :F/T], W2[:F/T, :], exactly
+    the shape every shard has) on the first 1024 tokens, i.e. 1/(T * N/1024)
+    of the step's FLOPs at the oracle's full BLAS efficiency (about 1 s)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     cfg = workload_config(args)
-    tokens = 32
+    tokens = min(1024, cfg.N)
     inp = gen_mlp_inputs(cfg, N=tokens)
-    W1 = oracle.mlp.as_f64(inp.W1)
-    W2 = oracle.mlp.as_f64(inp.W2)
+    Fs = cfg.Fs
+    X = oracle.mlp.as_f64(inp.X)
+    dY = oracle.mlp.as_f64(inp.dY)
+    W1 = oracle.mlp.as_f64(inp.W1[:, :Fs])
+    W2 = oracle.mlp.as_f64(inp.W2[:Fs, :])
 
     def step():
-        oracle.mlp.forward(inp.X, W1, None, W2, None, cfg.act)
-        oracle.mlp.backward(inp.X, W1, None, W2, inp.dY, cfg.act)
+        oracle.mlp.forward(X, W1, None, W2, None, cfg.act)
+        oracle.mlp.backward(X, W1, None, W2, dY, cfg.act)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    flops = 12.0 * tokens * cfg.D * cfg.F * args.steps
+    flops = 12.0 * tokens * cfg.D * Fs * args.steps
     value = flops / dt / 1e12
     cores = _cores()
-    sample = (f"{tokens} of {cfg.N} tokens per step, fwd+bwd, float64 numpy (OpenBLAS threads = "
-              f"host cores)")
+    sample = (f"shard 0 of {cfg.T} on {tokens} of {cfg.N} tokens per step (1/{cfg.T * cfg.N // tokens} "
+              f"of the step's FLOPs), fwd+bwd, float64 numpy (OpenBLAS threads = host cores)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
