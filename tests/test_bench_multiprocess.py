@@ -82,3 +82,22 @@ def test_kernel_source_hash_ignores_comments_but_not_code(monkeypatch, tmp_path)
     assert bench.kernel_source_hash("gemm") == h0
     f.write_text("// kernel\nint x = 2;  // one\n")
     assert bench.kernel_source_hash("gemm") != h0
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    """Rank 0 times the float64 oracle on a small shape and prints one line
+    with the contract's keys and the same `config` our arm prints."""
+    import json
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    args = bench.parse(["--impl", "reference", "--steps", "2", "--warmup", "1",
+                        "--shape", "96,256,512,4"])
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["steps"] == 2
+    assert line["config"] == bench.line_config(bench.workload_config(args), "splitk", 1)
+    assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert "96 of 96 tokens" in cb["sample"]
