@@ -18,7 +18,8 @@ Forms, asked of the library's own plan where the choice depends on the device:
   tiles: whole tiles of odd waves take their k-blocks from the last down
   (across the shard boundary of a folded K) and odd bands walk their tiles
   in reverse; the same block again with the plain ascending orders
-  (TPMLP_ALT_ORDER=0, in a fresh process);
+  (TPMLP_ALT_ORDER=0, in a fresh process); the reduce-scatter forward's
+  row-block epilogue over several waves and bands;
 - single-CTA 128-row tiles (65-128 token rows, 64-deep stages);
 - the cluster K split of 2, 3 and 4 CTAs (at most 64 token rows, no scratch);
 - stream-K (at most 64 token rows, with the scratch), and the part-wave
@@ -162,6 +163,34 @@ def test_cta_pair_plain_orders_bit_exact():
                         "-k", "test_cta_pair_128_deep_ring_long_k_ragged"],
                        env=env, cwd=root, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and "1 passed" in r.stdout, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_forward_reduce_scatter_over_waves_and_bands_bit_exact():
+    """The row GEMM's row-block epilogue (rank r's token rows written to its
+    own output buffer) over several waves and bands of pair tiles, where the
+    alternating K and band orders apply: each rank's rows equal the
+    unsharded definition's bit for bit, in both block-end modes (the
+    reduce-scatter block end, page 1 §04)."""
+    T = 4
+    N, D, Fs = 4096, 4104, 2056
+    bn, ctas, ks = tp.tpmlp_gemm_plan(N, D, Fs, T, fold=True, balanced=True)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    assert ctas == 2 and -(-N // 256) * -(-D // bn) > 2 * pairs and -(-N // 256) > 12
+    inp = gen_sparse_integer_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", seed=350, bias=True)
+    f, _ = expected(inp, bias_grads=False)
+    d = dev()
+    X = inp.X.to(d)
+    W1 = [w.to(d) for w in inp.W1_shards()]
+    W2 = [w.contiguous().to(d) for w in inp.W2_shards()]
+    b1 = [b.contiguous().to(d) for b in inp.b1_shards()]
+    b2 = inp.b2.to(d)
+    Ns = N // T
+    for mode in MODES:
+        Y_rows, _, _ = tp.mlp_forward_reduce_scatter(X, W1, W2, b1, b2, act="relu", mode=mode)
+        torch.cuda.synchronize()
+        for r in range(T):
+            np.testing.assert_array_equal(f64(Y_rows[r]), f["Y"][r * Ns:(r + 1) * Ns],
+                                          err_msg=f"rank {r} rows, {mode}")
 
 
 def test_single_cta_tiles_long_k_with_biases():
