@@ -919,17 +919,15 @@ def run_ours(args):
                        "regions": [rnd(flops_step * n_e / (m * 1e-3) / 1e12) for m in e_regions],
                        "compute_ms_per_step_median": e_compute,
                        "sm_mhz": eclk.get("sm_mhz"),
-                       "copies": "X, dY in and Y, dX out every step (pinned host memory, two copy "
-                                 "streams overlapped with compute, batches prefetched 3 steps ahead); weights "
-                                 "resident; value = the "
-                                 "median of 3 timed regions of `steps` steps (all in `regions`)"}
+                       "copies": "X, dY in, Y, dX out each step from/to pinned host memory on 2 "
+                                 "copy streams, 3 batches ahead; median of 3 regions"}
     if rank == 0 and not args.no_secondary and not args.shape:
         cb, cb_rel, cb_ratio = cublas_same_shapes(blk, args.steps, args.warmup, stream)
         line["cublas_same_shapes"] = {
             "value": rnd(cb), "unit": "TFLOP/s", "ours_over_cublas": rnd(cb_rel, 3),
             "per_gemm_ours_over_cublas": cb_ratio,
-            "note": "torch.matmul bf16 on the six unsharded products, alternating step by step "
-                    "with the library's step; plain products without the fused epilogues"}
+            "note": "torch.matmul bf16, the six unsharded products without epilogues, "
+                    "alternating with our step"}
     del blk
     torch.cuda.empty_cache()
     configs = None
