@@ -1,7 +1,7 @@
 // fp32 grouped / shard-folded GEMM on CUDA cores: the exact-fp32 mode of the
 // block (fmaf in fp32, no TF32 tensor cores, whose 10-bit mantissa would not
 // meet a 1e-5 relative bound). 64 x 64 output tile per CTA, 256 threads,
-// 4 x 4 outputs per thread, K staged through shared memory 32 at a time with
+// 4 x 4 adjacent outputs per thread, K staged through shared memory 32 at a time with
 // the next chunk's loads in flight in registers.
 // When the tiles are fewer than the SMs (the small blocks this mode is for),
 // a cluster of up to 8 CTAs shares one tile's K chunks; the leader adds the
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
     // A and B stages; after the K loop the first 16 KB hold this CTA's
     // partial tile for a K split
     __shared__ __align__(16) float stage[2 * TK * (TM + 4)];
-    __shared__ float Bs2[DUAL ? TK : 1][TN + 4];
+    __shared__ __align__(16) float Bs2[DUAL ? TK : 1][TN + 4];
     float (*As)[TM + 4] = reinterpret_cast<float (*)[TM + 4]>(stage);
     float (*Bs)[TN + 4] = reinterpret_cast<float (*)[TN + 4]>(stage + TK * (TM + 4));
     static_assert(2 * TK * (TM + 4) >= TM * TN, "partial tile fits in the stages");
@@ -139,19 +139,19 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
         if (c + 1 < c_hi) fetch(c + 1);
 #pragma unroll
         for (int kk = 0; kk < TK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+            // rows 4 ty .. 4 ty + 3 and columns 4 tx .. 4 tx + 3: one 16-byte
+            // shared load each (a warp reads 2 A and 16 B vectors)
+            const float4 av = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
+            const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+            const float a[4] = {av.x, av.y, av.z, av.w};
+            const float b[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
             if (DUAL) {
-                float b2[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) b2[j] = Bs2[kk][tx + 16 * j];
+                const float4 b2v = *reinterpret_cast<const float4*>(&Bs2[kk][4 * tx]);
+                const float b2[4] = {b2v.x, b2v.y, b2v.z, b2v.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -194,10 +194,10 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
     const int g_out = p.fold ? 0 : gz;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int m = m0 + ty + 16 * i;
+        const int m = m0 + 4 * ty + i;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx + 16 * j;
+            const int n = n0 + 4 * tx + j;
             if (m < p.M && n < p.N) {
                 if (DUAL)
                     epi_swiglu_scalar(p.epi, g_out, m, n, acc[i][j], acc2[i][j]);
