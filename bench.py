@@ -78,6 +78,9 @@ def parse(argv=None):
                          "tokens (small cases for profiling)")
     ap.add_argument("--only-decode", action="store_true",
                     help="time only the weight-streaming forward (N=16 D=12288 F=49152 T=8)")
+    ap.add_argument("--only-bias-grads", action="store_true",
+                    help="time only the bias-gradient column sums of the fwd+bwd workload "
+                         "(with --shape: of that shape)")
     ap.add_argument("--only-f32", action="store_true",
                     help="time only the exact-fp32 block (N=64 D=256 F=1024 T=2, ReLU, biases), "
                          "forward and forward + backward")
@@ -574,6 +577,24 @@ def measure_embedding(dev, iters, pk):
     return e
 
 
+def measure_bias_grads(blk, iters, stream, pk):
+    """Bias gradients db1^(r) = sum_n dZ^(r) and db2 = sum_n dY of a block whose
+    forward has run: the backward's column sums (a launch over the T dZ shards
+    and one over dY), GB/s of the bytes they read and write per call."""
+    import tensor_transformer_mlp_columnparallel_gb300 as tp
+    cfg, dev = blk.cfg, blk.dev
+    db1 = [torch.empty(cfg.Fs, dtype=torch.bfloat16, device=dev) for _ in range(cfg.T)]
+    db2 = torch.empty(cfg.D, dtype=torch.bfloat16, device=dev)
+
+    def bwd_bias():
+        tp.tpmlp_backward(blk.X, blk.W1, blk.W2, blk.H, blk.Z, blk.dY, blk.dX, blk.dW1, blk.dW2,
+                          db1, db2, cfg.act, blk.mode, blk.ws)
+    _, _, t = _lib_timed(tp, bwd_bias, iters, stream)
+    ms = t["bias_grad_colsum"]["total_ms"] / iters   # per backward call
+    nbytes = cfg.N * (cfg.F + cfg.D) * 2.0 + (cfg.F + cfg.D) * 2.0
+    return _hbm_entry(nbytes / (ms * 1e-3) / 1e9, ms, pk, "bias_grad_colsum")
+
+
 def measure_configs(dev, stream, iters, pk, detail):
     """Every named workload besides the headline step. Returns the compact
     map of the JSON line; per-kernel tables go into `detail`."""
@@ -631,6 +652,7 @@ def measure_configs(dev, stream, iters, pk, detail):
     for name, short in (("block_reduce_bias", "reduce_y"), ("block_reduce_dx", "reduce_dx")):
         rms = _kernel_ms(t, name)
         rec[short] = _hbm_entry(rb / (rms * 1e-3) / 1e9, rms, pk, name)
+    rec["bias_grads"] = measure_bias_grads(blk, max(5, iters // 4), stream, pk)
     out["c3 fwd+bwd N8192 D8192 F28672 T8"] = rec
     del blk
     torch.cuda.empty_cache()
@@ -1018,6 +1040,12 @@ def run_only(args):
                "results": measure_ce(dev, stream, iters, pk, args.only_ce)}
     elif args.only_embedding:
         res = {"only": "vocab_embedding", "results": measure_embedding(dev, iters, pk)}
+    elif args.only_bias_grads:
+        cfg = workload_config(args)
+        blk = Block(cfg, args.mode, dev)
+        blk.step()
+        res = {"only": "bias_grads", "workload": cfg.name,
+               "results": measure_bias_grads(blk, max(5, iters // 4), stream, pk)}
     elif args.only_f32:
         import tensor_transformer_mlp_columnparallel_gb300 as tp
         fb = Block(MLP_CONFIGS["mlp_f32_relu_n64_d256_f1024_t2"], args.mode, dev)
@@ -1039,7 +1067,8 @@ def run_only(args):
 
 def main():
     args = parse()
-    if args.only_ce or args.only_embedding or args.only_decode or args.only_f32:
+    if (args.only_ce or args.only_embedding or args.only_decode or args.only_f32
+            or args.only_bias_grads):
         run_only(args)
         return
     if args.impl == "reference":

@@ -597,13 +597,35 @@ tpmlp_status tpmlp_backward(tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int
         TPMLP_TRY(run_gemm(dt, g4, s, sk));
     }
 
-    // 5. bias gradients
-    if (db1 != nullptr)
-        TPMLP_TRY(run_colsum(f32, N, Fs, Fs, T, reinterpret_cast<const void* const*>(dZ), db1, s));
-    if (db2 != nullptr) {
-        const void* in[1] = {dY};
-        void* out[1] = {db2};
-        TPMLP_TRY(run_colsum(f32, N, D, D, 1, in, out, s));
+    // 5. bias gradients: the column sums of the T dZ shards (db1) and of dY
+    // (db2). With the stream-K scratch of a balanced workspace (free once the
+    // GEMMs above are done: same stream) they stream whole rows in two
+    // passes through it, all groups at once; without it one pass per column
+    // strip, dZ's shards and dY in separate launches.
+    {
+        const void* in[kMaxColsumG];
+        void* out[kMaxColsumG];
+        int64_t cols[kMaxColsumG], ld[kMaxColsumG];
+        int G = 0;
+        if (db1 != nullptr)
+            for (int r = 0; r < T; ++r, ++G) {
+                in[G] = dZ[r];
+                out[G] = db1[r];
+                cols[G] = ld[G] = Fs;
+            }
+        if (db2 != nullptr) {
+            in[G] = dY;
+            out[G] = db2;
+            cols[G] = ld[G] = D;
+            ++G;
+        }
+        if (G > 0 && sk.part != nullptr && !f32) {
+            TPMLP_TRY(run_colsum(f32, N, G, cols, ld, in, out, s, sk.part, sk.part_bytes));
+        } else {
+            const int Gz = db1 != nullptr ? T : 0;
+            if (Gz > 0) TPMLP_TRY(run_colsum(f32, N, Gz, cols, ld, in, out, s));
+            if (db2 != nullptr) TPMLP_TRY(run_colsum(f32, N, 1, cols + Gz, ld + Gz, in + Gz, out + Gz, s));
+        }
     }
     return TPMLP_OK;
 }

@@ -164,9 +164,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // ---------------------------------------------------------------- colsum --
 
 struct ColsumParams {
-    const void* in[kMaxG];
-    void* out[kMaxG];
-    int64_t rows, cols, ld;
+    const void* in[kMaxColsumG];
+    void* out[kMaxColsumG];
+    int64_t cols[kMaxColsumG], ld[kMaxColsumG];
+    int64_t colbase[kMaxColsumG];   // two-pass form: the group's first column in the scratch rows
+    int rng0[kMaxColsumG + 1];      // two-pass form: the group's first column range (grid x)
+    int64_t rows, total_cols;
+    int G, S;                       // two-pass form: row chunks (grid y)
+    float* scratch;                 // two-pass form: S rows of total_cols partial sums
 };
 
 template <typename T>
@@ -175,19 +180,20 @@ __global__ void __launch_bounds__(256) colsum_kernel(const ColsumParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = blockIdx.y;
     const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    const int64_t cols = p.cols[g], ld = p.ld[g];
     float s = 0.f;
-    if (c < p.cols) {
+    if (c < cols) {
         const T* in = static_cast<const T*>(p.in[g]);
         for (int64_t r = warp; r < p.rows; r += 8) {
             if constexpr (sizeof(T) == 4)
-                s += in[r * p.ld + c];
+                s += in[r * ld + c];
             else
-                s += __bfloat162float(in[r * p.ld + c]);
+                s += __bfloat162float(in[r * ld + c]);
         }
     }
     red[warp][lane] = s;
     __syncthreads();
-    if (warp == 0 && c < p.cols) {
+    if (warp == 0 && c < cols) {
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) t += red[w][lane];
@@ -196,6 +202,159 @@ __global__ void __launch_bounds__(256) colsum_kernel(const ColsumParams p) {
         else
             static_cast<__nv_bfloat16*>(p.out[g])[c] = __float2bfloat16_rn(t);
     }
+}
+
+// Single-pass form for 16-byte aligned rows (the bf16 path without scratch
+// space, fp32 when the columns and pitch allow): each CTA owns a strip of
+// CS_COLS columns of one group (grid x) and all its rows. A lane reads one 16-byte vector (VEC columns)
+// of a row, the lanes of a warp cover RPW rows at once, the 8 warps PHASES
+// rows, and each thread keeps UNROLL such loads in flight before adding
+// them: 8 when the strips alone fill the GPU several times over, 16 when they
+// are few (dY's), so that the resident CTAs keep enough bytes moving to
+// stream at HBM rate. (Splitting rows across a CTA cluster instead measured
+// far slower.) Every column's sum is formed in a fixed order (each thread's
+// rows in increasing order, then the row phases in turn), so results do not
+// depend on timing.
+constexpr int CS_THREADS = 256;
+constexpr int CS_COLS = 32;      // columns per strip
+
+template <typename T, int UNROLL>
+__global__ void __launch_bounds__(CS_THREADS) colsum_vec_kernel(const ColsumParams p) {
+    constexpr int VEC = 16 / (int)sizeof(T);         // columns per 16-byte vector
+    constexpr int LPR = CS_COLS / VEC;               // lanes per row
+    constexpr int RPW = 32 / LPR;                    // rows per warp load
+    constexpr int PHASES = (CS_THREADS / 32) * RPW;  // rows covered by one load of every thread
+    __shared__ float part[PHASES][CS_COLS + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int slot = lane % LPR;                     // which vector of the strip
+    const int phase = warp * RPW + lane / LPR;       // this thread's first row
+    const int g = blockIdx.y;
+    const int strip = blockIdx.x;
+    const int64_t cols = p.cols[g], ld = p.ld[g];
+    const int64_t c0 = (int64_t)strip * CS_COLS + slot * VEC;
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    if (c0 < cols) {
+        const T* in = static_cast<const T*>(p.in[g]) + c0;
+        for (int64_t base = phase; base < p.rows; base += (int64_t)PHASES * UNROLL) {
+            uint4 w[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t r = base + (int64_t)u * PHASES;
+                w[u] = r < p.rows ? __ldcs(reinterpret_cast<const uint4*>(in + r * ld))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                if constexpr (sizeof(T) == 4) {
+                    acc[0] += __uint_as_float(w[u].x);
+                    acc[1] += __uint_as_float(w[u].y);
+                    acc[2] += __uint_as_float(w[u].z);
+                    acc[3] += __uint_as_float(w[u].w);
+                } else {
+                    const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] += __uint_as_float(ws[q] << 16);
+                        acc[2 * q + 1] += __uint_as_float(ws[q] & 0xffff0000u);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) part[phase][slot * VEC + v] = acc[v];
+    __syncthreads();
+    if (threadIdx.x < CS_COLS) {
+        const int64_t c = (int64_t)strip * CS_COLS + threadIdx.x;
+        if (c < cols) {
+            float t = 0.f;
+            for (int ph = 0; ph < PHASES; ++ph) t += part[ph][threadIdx.x];
+            if constexpr (sizeof(T) == 4)
+                static_cast<float*>(p.out[g])[c] = t;
+            else
+                static_cast<__nv_bfloat16*>(p.out[g])[c] = __float2bfloat16_rn(t);
+        }
+    }
+}
+
+// Two-pass form (bf16, with scratch space). Pass 1: CTA (x, y) sums row chunk
+// y (a contiguous 1/S of the rows) of column range x, up to CP_COLS columns
+// of one group: thread t owns the 16-byte vectors t and t + 256 of each row,
+// so the CTA reads a contiguous stretch of up to 8 KB of every row (a dZ
+// shard's whole row: one contiguous block over its rows), CP_UNROLL rows in
+// flight; each thread writes its column sums to row y of the scratch.
+// (Reading narrow strips down all rows instead, one 64-byte piece of every
+// row per CTA, left DRAM at about 3 TB/s; this form reaches about 4.)
+// Pass 2: one thread per column adds the S chunk sums in chunk order. Fixed
+// order throughout, so results do not depend on timing.
+constexpr int CP_THREADS = 256;
+constexpr int CP_VPT = 2;                          // 16-byte vectors per thread and row
+constexpr int CP_COLS = CP_THREADS * 8 * CP_VPT;   // bf16 columns per range
+constexpr int CP_UNROLL = 2;
+
+__global__ void __launch_bounds__(CP_THREADS) colsum_part_kernel(const ColsumParams p) {
+    int g = 0;
+    while (g + 1 < p.G && (int)blockIdx.x >= p.rng0[g + 1]) ++g;
+    const int64_t c_start = (int64_t)((int)blockIdx.x - p.rng0[g]) * CP_COLS;
+    const int64_t cols = p.cols[g], ld = p.ld[g];
+    const int chunk = blockIdx.y;
+    const int64_t r_lo = p.rows * chunk / p.S, r_hi = p.rows * (chunk + 1) / p.S;
+    const __nv_bfloat16* in = static_cast<const __nv_bfloat16*>(p.in[g]);
+    bool on[CP_VPT];
+    int64_t c[CP_VPT];
+#pragma unroll
+    for (int k = 0; k < CP_VPT; ++k) {
+        c[k] = c_start + (int64_t)(threadIdx.x + CP_THREADS * k) * 8;
+        on[k] = c[k] < cols;
+    }
+    if (!on[0]) return;   // no barrier follows
+    float acc[CP_VPT][8];
+#pragma unroll
+    for (int k = 0; k < CP_VPT; ++k)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) acc[k][v] = 0.f;
+    for (int64_t base = r_lo; base < r_hi; base += CP_UNROLL) {
+        uint4 w[CP_UNROLL][CP_VPT];
+#pragma unroll
+        for (int u = 0; u < CP_UNROLL; ++u)
+#pragma unroll
+            for (int k = 0; k < CP_VPT; ++k) {
+                const int64_t r = base + u;
+                w[u][k] = (r < r_hi && on[k])
+                              ? __ldcs(reinterpret_cast<const uint4*>(in + r * ld + c[k]))
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+        for (int u = 0; u < CP_UNROLL; ++u)
+#pragma unroll
+            for (int k = 0; k < CP_VPT; ++k) {
+                const uint32_t ws[4] = {w[u][k].x, w[u][k].y, w[u][k].z, w[u][k].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[k][2 * q] += __uint_as_float(ws[q] << 16);
+                    acc[k][2 * q + 1] += __uint_as_float(ws[q] & 0xffff0000u);
+                }
+            }
+    }
+#pragma unroll
+    for (int k = 0; k < CP_VPT; ++k) {
+        if (!on[k]) continue;
+        float4* dst = reinterpret_cast<float4*>(p.scratch + chunk * p.total_cols + p.colbase[g] + c[k]);
+        dst[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+        dst[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+}
+
+__global__ void __launch_bounds__(256) colsum_final_kernel(const ColsumParams p) {
+    const int64_t col = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (col >= p.total_cols) return;
+    int g = 0;
+    while (g + 1 < p.G && col >= p.colbase[g + 1]) ++g;
+    float t = 0.f;
+    for (int chunk = 0; chunk < p.S; ++chunk) t += p.scratch[chunk * p.total_cols + col];
+    static_cast<__nv_bfloat16*>(p.out[g])[col - p.colbase[g]] = __float2bfloat16_rn(t);
 }
 
 // -------------------------------------------------------------- vocab CE --
@@ -623,24 +782,77 @@ tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const fl
     return e == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }
 
-tpmlp_status run_colsum(int f32, int64_t rows, int64_t cols, int64_t ld, int G,
-                        const void* const* in, void* const* out, cudaStream_t s) {
-    if (cols == 0 || G == 0) return TPMLP_OK;
+tpmlp_status run_colsum(int f32, int64_t rows, int G, const int64_t* cols, const int64_t* ld,
+                        const void* const* in, void* const* out, cudaStream_t s, float* scratch,
+                        size_t scratch_bytes) {
+    if (G <= 0) return TPMLP_OK;
+    if (G > kMaxColsumG) return TPMLP_ERR_SHAPE;
     ColsumParams kp{};
+    kp.rows = rows;
+    kp.G = G;
+    // the vector forms need every row's vectors 16-byte aligned
+    const int vec = f32 ? 4 : 8;
+    bool vec_ok = true;
+    int64_t max_cols = 0, total = 0, ranges = 0;
     for (int g = 0; g < G; ++g) {
         kp.in[g] = in[g];
         kp.out[g] = out[g];
+        kp.cols[g] = cols[g];
+        kp.ld[g] = ld[g];
+        kp.colbase[g] = total;
+        kp.rng0[g] = (int)ranges;
+        total += cols[g];
+        ranges += (cols[g] + CP_COLS - 1) / CP_COLS;
+        max_cols = cols[g] > max_cols ? cols[g] : max_cols;
+        vec_ok = vec_ok && cols[g] % vec == 0 && ld[g] % vec == 0 && aligned16(in[g]);
     }
-    kp.rows = rows;
-    kp.cols = cols;
-    kp.ld = ld;
-    dim3 grid((unsigned)((cols + 31) / 32), (unsigned)G);
+    kp.rng0[G] = (int)ranges;
+    kp.total_cols = total;
+    if (max_cols == 0) return TPMLP_OK;
+    // two-pass form: row chunks for about 8 CTAs per SM in pass 1 (at most
+    // 64 chunks, each at least 64 rows, the partials within the scratch). On
+    // the fwd+bwd shape's sums (10 ranges) 64 chunks took 0.155 ms, 60 took
+    // 0.165, 30 took 0.29; 1 to 4 rows in flight per thread were within 2%,
+    // 8 or 16 took 0.29.
+    int S = 0;
+    if (!f32 && vec_ok && scratch != nullptr && aligned16(scratch) && rows >= 64 && ranges > 0) {
+        int64_t sc = 8 * (int64_t)device_sm_count() / ranges;
+        sc = sc < 1 ? 1 : (sc > 64 ? 64 : sc);
+        if (sc > rows / 64) sc = rows / 64;
+        while (sc > 0 && (size_t)sc * (size_t)total * sizeof(float) > scratch_bytes) --sc;
+        S = (int)sc;
+    }
     {
         LaunchScope ls("bias_grad_colsum", s);
-        if (f32)
-            colsum_kernel<float><<<grid, 256, 0, s>>>(kp);
-        else
-            colsum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(kp);
+        if (S >= 1) {
+            kp.S = S;
+            kp.scratch = scratch;
+            colsum_part_kernel<<<dim3((unsigned)ranges, (unsigned)S), CP_THREADS, 0, s>>>(kp);
+            colsum_final_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(kp);
+        } else if (vec_ok) {
+            // deeper per-thread load queues when the strips are few (under
+            // two per SM), so the resident CTAs still keep HBM busy
+            const int64_t strips = (max_cols + CS_COLS - 1) / CS_COLS;
+            const bool few = strips * G < 2 * (int64_t)device_sm_count();
+            const dim3 grid((unsigned)strips, (unsigned)G);
+            if (f32) {
+                if (few)
+                    colsum_vec_kernel<float, 16><<<grid, CS_THREADS, 0, s>>>(kp);
+                else
+                    colsum_vec_kernel<float, 8><<<grid, CS_THREADS, 0, s>>>(kp);
+            } else {
+                if (few)
+                    colsum_vec_kernel<__nv_bfloat16, 16><<<grid, CS_THREADS, 0, s>>>(kp);
+                else
+                    colsum_vec_kernel<__nv_bfloat16, 8><<<grid, CS_THREADS, 0, s>>>(kp);
+            }
+        } else {
+            dim3 grid((unsigned)((max_cols + 31) / 32), (unsigned)G);
+            if (f32)
+                colsum_kernel<float><<<grid, 256, 0, s>>>(kp);
+            else
+                colsum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(kp);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }

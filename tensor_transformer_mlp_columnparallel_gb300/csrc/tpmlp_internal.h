@@ -88,9 +88,14 @@ tpmlp_status run_block_reduce(int out_f32, int64_t N, int64_t D, int T, const fl
 tpmlp_status run_vocab_embedding(int f32, int64_t N, int64_t V, int64_t H, int T,
                                  const int64_t* ids, const void* const* table, void* out,
                                  cudaStream_t s);
-// out_g[c] = sum_r in_g[r * ld + c] for G groups (bias gradients).
-tpmlp_status run_colsum(int f32, int64_t rows, int64_t cols, int64_t ld, int G,
-                        const void* const* in, void* const* out, cudaStream_t s);
+// out_g[c] = sum_r in_g[r * ld_g + c], c < cols_g, for G <= kMaxColsumG groups
+// of `rows` rows each (bias gradients: the T dZ shards and dY). With fp32
+// scratch space (scratch_bytes, 16-byte aligned; bf16 only) the sums stream
+// whole rows in two passes through it, else one pass per column strip.
+constexpr int kMaxColsumG = kMaxG + 1;
+tpmlp_status run_colsum(int f32, int64_t rows, int G, const int64_t* cols, const int64_t* ld,
+                        const void* const* in, void* const* out, cudaStream_t s,
+                        float* scratch = nullptr, size_t scratch_bytes = 0);
 tpmlp_status run_vocab_ce(int64_t N, int64_t V, int T, const float* logits,
                           const int64_t* targets, float* loss, float* loss_mean, int32_t* argmax,
                           int32_t* owner, cudaStream_t s);
