@@ -19,7 +19,8 @@ Forms, asked of the library's own plan where the choice depends on the device:
   (across the shard boundary of a folded K) and odd bands walk their tiles
   in reverse; the same block again with the plain ascending orders
   (TPMLP_ALT_ORDER=0, in a fresh process); the reduce-scatter forward's
-  row-block epilogue over several waves and bands;
+  row-block epilogue over several waves and bands; the bias-gradient
+  column sums in two passes and in one;
 - single-CTA 128-row tiles (65-128 token rows, 64-deep stages);
 - the cluster K split of 2, 3 and 4 CTAs (at most 64 token rows, no scratch);
 - stream-K (at most 64 token rows, with the scratch), and the part-wave
@@ -191,6 +192,23 @@ def test_forward_reduce_scatter_over_waves_and_bands_bit_exact():
         for r in range(T):
             np.testing.assert_array_equal(f64(Y_rows[r]), f["Y"][r * Ns:(r + 1) * Ns],
                                           err_msg=f"rank {r} rows, {mode}")
+
+
+def test_bias_gradient_column_sums_bit_exact():
+    """db1 = sum_n dZ^(r) and db2 = sum_n dY over 1100 token rows, with dZ
+    shard rows and dY rows of 4104 columns: with the balanced workspace the
+    two passes through the scratch (two column ranges per row, the second
+    8 columns wide, and 17 uneven row chunks), with the plain workspace the
+    one-pass strips; both equal to the oracle bit for bit."""
+    T, N, D, Fs = 2, 1100, 4104, 4104
+    inp = gen_sparse_integer_mlp(N=N, D=D, F=T * Fs, T=T, dtype="bf16", seed=360,
+                                 density=(0.1, 0.02, 0.02, 0.05), bias=True)
+    f, g = expected(inp, bias_grads=True)
+    assert np.mean(g["db1"] != 0) > 0.5 and np.mean(g["db2"] != 0) > 0.5
+    for mode in MODES:
+        for balanced in (True, False):
+            assert_exact(inp, run_block(inp, mode, balanced, True), f, g,
+                         f"bias grads {mode} bal={balanced}")
 
 
 def test_single_cta_tiles_long_k_with_biases():
