@@ -206,15 +206,15 @@ __global__ void __launch_bounds__(256) colsum_kernel(const ColsumParams p) {
 
 // Single-pass form for 16-byte aligned rows (the bf16 path without scratch
 // space, fp32 when the columns and pitch allow): each CTA owns a strip of
-// CS_COLS columns of one group (grid x) and all its rows. A lane reads one 16-byte vector (VEC columns)
-// of a row, the lanes of a warp cover RPW rows at once, the 8 warps PHASES
-// rows, and each thread keeps UNROLL such loads in flight before adding
-// them: 8 when the strips alone fill the GPU several times over, 16 when they
-// are few (dY's), so that the resident CTAs keep enough bytes moving to
-// stream at HBM rate. (Splitting rows across a CTA cluster instead measured
-// far slower.) Every column's sum is formed in a fixed order (each thread's
-// rows in increasing order, then the row phases in turn), so results do not
-// depend on timing.
+// CS_COLS columns of one group (grid x: strip, y: group) and all its rows. A
+// lane reads one 16-byte vector (VEC columns) of a row, the lanes of a warp
+// cover RPW rows at once, the 8 warps PHASES rows, and each thread keeps
+// UNROLL such loads in flight before adding them: 8 when the strips fill the
+// GPU twice over, else 16 (dY's), so that the resident CTAs keep more bytes
+// moving. (Splitting rows across a CTA cluster instead measured slower.)
+// Every column's sum is formed in a fixed order (each thread's rows in
+// increasing order, then the row phases in turn), so results do not depend
+// on timing.
 constexpr int CS_THREADS = 256;
 constexpr int CS_COLS = 32;      // columns per strip
 
