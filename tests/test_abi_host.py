@@ -196,3 +196,17 @@ def test_gemm_stall_self_test_role_is_checked(lib):
     assert lib.tpmlp_selftest_gemm_stall(-1) == B.ERR_ARG
     for role in (1, 2, 3, 0):
         assert lib.tpmlp_selftest_gemm_stall(role) == B.OK
+
+
+def test_every_environment_switch_is_documented_in_the_header():
+    """The library's sources read only environment variables that the public
+    header describes (launch-order switches that never change results)."""
+    csrc = os.path.join(ROOT, "tensor_transformer_mlp_columnparallel_gb300", "csrc")
+    names = set()
+    for f in os.listdir(csrc):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            names |= set(re.findall(r'getenv\("([A-Z0-9_]+)"\)', open(os.path.join(csrc, f)).read()))
+    assert names, "no environment switches found"
+    header = open(os.path.join(ROOT, "include", "tpmlp.h")).read()
+    for n in sorted(names):
+        assert n in header, n
