@@ -270,22 +270,28 @@ tpmlp_status tpmlp_forward_noalloc(tpmlp_dtype dt, int64_t N, int64_t D, int64_t
 size_t tpmlp_workspace_bytes(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D, int64_t F, int T,
                              tpmlp_reduce_mode mode);
 
-/* Workspace bytes that also hold the optional scratch of the few-token
- * GEMMs (bf16, 1 <= N <= 64; for other arguments the same as
- * tpmlp_workspace_bytes). The scratch starts at round_up(required, 256)
- * bytes: per-tile arrival counters and fp32 partial accumulators of up to
- * 256 CTAs. Given a workspace of at least this size (16-byte aligned; for a
- * SPLITK forward this is the only use of the workspace), the GEMMs whose M
- * is the token count (the column GEMM, the row GEMM, dZ, dX) may run in the
- * stream-K form: every SM streams the same number of k-blocks, and a tile
- * whose K range two or more CTAs share is summed through the scratch, in
- * CTA order, by the last CTA to finish it (no CTA waits for another; the
- * result does not depend on timing). A smaller workspace (down to the
- * required size) runs the same GEMMs without the scratch, with a different
- * order of fp32 additions. The counters are reset on the call's stream
- * before each use; what the scratch held before is never read.
- * Returns (size_t)-1 for invalid shapes. Library extension; the source
- * pages have no counterpart. */
+/* Workspace bytes that also hold the optional fp32 scratch of the bf16 path
+ * (bf16 and N >= 1; for other arguments the same as tpmlp_workspace_bytes).
+ * The scratch starts at round_up(required, 256) bytes: per-tile arrival
+ * counters, then partial accumulators. Given a workspace of at least this
+ * size (16-byte aligned; for a SPLITK forward this is the only use of the
+ * workspace):
+ * - with at most 64 tokens, the GEMMs whose M is the token count (the
+ *   column GEMM, the row GEMM, dZ, dX) may run in the stream-K form: every
+ *   SM streams the same number of k-blocks, and a tile whose K range two or
+ *   more CTAs share is summed through the scratch, in CTA order, by the last
+ *   CTA to finish it (no CTA waits for another);
+ * - with more, a GEMM whose last wave of tiles would leave SMs idle cuts
+ *   those tiles into equal K chunks run side by side and summed the same
+ *   way;
+ * - the backward's bias gradients (db1, db2), which run after its GEMMs,
+ *   sum row chunks of contiguous column ranges into the scratch and then
+ *   add the chunks in order.
+ * Results do not depend on timing. A smaller workspace (down to the required
+ * size) runs the same calls without the scratch, with a different order of
+ * fp32 additions. The counters are reset on the call's stream before each
+ * use; what the scratch held before is never read. Returns (size_t)-1 for
+ * invalid shapes. Library extension; the source pages have no counterpart. */
 size_t tpmlp_workspace_bytes_balanced(tpmlp_op op, tpmlp_dtype dt, int64_t N, int64_t D,
                                       int64_t F, int T, tpmlp_reduce_mode mode);
 
